@@ -1,0 +1,110 @@
+"""Masked softmax attention over a paged E5M2 KV cache, in float64.
+
+Test infrastructure only (see the package docstring).
+
+What it computes is the plain definition of one decode step of grouped-query
+attention (page "[Kernel][SM70] Pipeline batched E5M2 XQA decode", section
+"Purpose": batched long-context XQA decode on an FP8 E5M2 KV cache; section
+"Pending work and gates": randomized-page operator checks, boundary contexts).
+The pages print no formula, so the following readings are taken:
+
+* q head ``h`` reads kv head ``h // G`` with ``G = Hq / Hkv`` (consecutive groups);
+* logical token ``t`` of sequence ``b`` lives in physical page
+  ``block_tables[b, t // BS]``, slot ``t % BS``; cache layout [NB, Hkv, BS, D];
+* ``k = k_scale * decode(K code)``, ``v = v_scale * decode(V code)``;
+* ``s_t = sm_scale * <q, k_t>`` with ``sm_scale = 1/sqrt(D)`` unless given;
+* ``out = sum_t softmax(s)_t v_t`` over ``t < ctx_b`` only (tokens past the
+  context are never read); ``ctx_b == 0`` gives a zero output row.
+
+The result is the exact attention value up to float64 rounding, not an
+approximation; the output is left in float64 (no fp16 rounding).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import e5m2
+
+
+def gather_sequence_kv(cache: np.ndarray, block_tables: np.ndarray, b: int, ctx: int, kv_head: int) -> np.ndarray:
+    """Codes of tokens 0..ctx-1 of sequence ``b``, kv head ``kv_head``: uint8 [ctx, D]."""
+    num_blocks, _, bs, d = cache.shape
+    npages = (ctx + bs - 1) // bs
+    pages = np.asarray(block_tables[b, :npages], dtype=np.int64)
+    if np.any(pages < 0) or np.any(pages >= num_blocks):
+        raise ValueError(f"sequence {b}: block id out of range in the first {npages} table entries")
+    return cache[pages, kv_head].reshape(npages * bs, d)[:ctx]
+
+
+def paged_decode_attention(
+    q: np.ndarray,
+    k_cache: np.ndarray,
+    v_cache: np.ndarray,
+    block_tables: np.ndarray,
+    context_lens: np.ndarray,
+    k_scale: float,
+    v_scale: float,
+    sm_scale: float | None = None,
+) -> np.ndarray:
+    """One decode step: float64 [B, Hq, D] attention output."""
+    batch, hq, d = q.shape
+    _, hkv, _, d2 = k_cache.shape
+    if d2 != d or hq % hkv != 0:
+        raise ValueError("shape mismatch")
+    group = hq // hkv
+    if sm_scale is None or sm_scale <= 0.0:
+        sm_scale = 1.0 / math.sqrt(d)
+    table = e5m2.lut()
+    out = np.zeros((batch, hq, d), dtype=np.float64)
+    for b in range(batch):
+        ctx = int(context_lens[b])
+        if ctx < 0:
+            raise ValueError("negative context length")
+        if ctx == 0:
+            continue
+        for g in range(hkv):
+            k = float(k_scale) * table[gather_sequence_kv(k_cache, block_tables, b, ctx, g)]
+            v = float(v_scale) * table[gather_sequence_kv(v_cache, block_tables, b, ctx, g)]
+            heads = slice(g * group, (g + 1) * group)
+            qh = q[b, heads].astype(np.float64)
+            s = float(sm_scale) * (qh @ k.T)  # [G, ctx]
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            p = p / p.sum(axis=1, keepdims=True)
+            out[b, heads] = p @ v
+    return out
+
+
+def paged_decode_attention_rows(
+    q: np.ndarray,
+    k_cache: np.ndarray,
+    v_cache: np.ndarray,
+    block_tables: np.ndarray,
+    context_lens: np.ndarray,
+    k_scale: float,
+    v_scale: float,
+    rows,
+    sm_scale: float | None = None,
+) -> np.ndarray:
+    """The same definition evaluated for selected (b, h) rows only: float64 [len(rows), D]."""
+    batch, hq, d = q.shape
+    hkv = k_cache.shape[1]
+    group = hq // hkv
+    if sm_scale is None or sm_scale <= 0.0:
+        sm_scale = 1.0 / math.sqrt(d)
+    table = e5m2.lut()
+    res = np.zeros((len(rows), d), dtype=np.float64)
+    for i, (b, h) in enumerate(rows):
+        ctx = int(context_lens[b])
+        if ctx == 0:
+            continue
+        g = h // group
+        k = float(k_scale) * table[gather_sequence_kv(k_cache, block_tables, b, ctx, g)]
+        v = float(v_scale) * table[gather_sequence_kv(v_cache, block_tables, b, ctx, g)]
+        s = float(sm_scale) * (k @ q[b, h].astype(np.float64))
+        s = s - s.max()
+        p = np.exp(s)
+        res[i] = (p / p.sum()) @ v
+    return res

@@ -1,0 +1,102 @@
+"""Integer definition of the split-KV work partition.
+
+Test infrastructure only (see the package docstring).
+
+The page "[Kernel][WIP] Follow up FlashNext batch HC fusion and QSA route audit"
+(section "Test Result") structures split-KV attention as planner -> forward ->
+merge, and records that a capacity-sized grid leaves CTAs empty on short
+contexts while fixed grids or contiguous grouping regress long contexts, and
+that too few CTAs is catastrophic. The pages give no partition rule; the one
+this build adopts (a reading) sizes every split from the total work:
+
+* a *segment* is one (sequence b, kv head g) pair, index ``s = b*Hkv + g``; it
+  holds ``ceil(ctx_b / BS)`` pages (0 if ``ctx_b`` is 0 or invalid);
+* segments are laid end to end, ``seg_start`` is the exclusive prefix sum of
+  their page counts and ``P = seg_start[-1]`` is the total;
+* the number of CTAs is ``n = 0`` if ``P == 0`` else
+  ``min(max_ctas, max(1, ceil(P / min_pages_per_cta)))``;
+* CTA ``i`` owns the flattened pages ``[floor(i*P/n), floor((i+1)*P/n))``, so
+  shares differ by at most one page whatever the length mix: long sequences are
+  split across CTAs, short ones share a CTA;
+* the intersection of CTA ``i`` with segment ``s`` is a *piece*; its partial
+  result slot is ``i + s`` (unique, since walking the flattened order every
+  piece boundary advances ``i`` or ``s``).
+
+A context length outside ``[0, MBS*BS]`` marks the segment bad (0 pages).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def segment_pages(context_lens, num_kv_heads: int, max_blocks_per_seq: int, block_size: int = 16):
+    """Pages per segment and the bad-segment flags: (int64 [B*Hkv], bool [B*Hkv])."""
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    bad_seq = (ctx < 0) | (ctx > int(max_blocks_per_seq) * block_size)
+    pages_seq = np.where(bad_seq, 0, (ctx + block_size - 1) // block_size)
+    pages = np.repeat(pages_seq, num_kv_heads)
+    bad = np.repeat(bad_seq, num_kv_heads)
+    return pages.astype(np.int64), bad
+
+
+def segment_starts(pages) -> np.ndarray:
+    """Exclusive prefix sum with the total appended: int64 [nseg + 1]."""
+    pages = np.asarray(pages, dtype=np.int64)
+    out = np.zeros(pages.shape[0] + 1, dtype=np.int64)
+    out[1:] = np.cumsum(pages)
+    return out
+
+
+def num_ctas(total_pages: int, max_ctas: int, min_pages_per_cta: int) -> int:
+    if total_pages <= 0:
+        return 0
+    want = -(-int(total_pages) // int(min_pages_per_cta))
+    return int(min(int(max_ctas), max(1, want)))
+
+
+def cta_range(i: int, total_pages: int, n: int):
+    """Flattened page range [begin, end) of CTA ``i``."""
+    return (i * total_pages) // n, ((i + 1) * total_pages) // n
+
+
+def cta_of_page(p: int, total_pages: int, n: int) -> int:
+    """The CTA whose range holds flattened page ``p`` (closed form)."""
+    return ((p + 1) * n - 1) // total_pages
+
+
+def pieces(seg_start, n: int):
+    """All (cta, segment, page_begin, page_end, slot) pieces, in flattened order."""
+    seg_start = np.asarray(seg_start, dtype=np.int64)
+    total = int(seg_start[-1])
+    out = []
+    for i in range(n):
+        a, e = cta_range(i, total, n)
+        if a == e:
+            continue
+        s = int(np.searchsorted(seg_start, a, side="right") - 1)
+        while a < e:
+            seg_end = int(seg_start[s + 1])
+            if seg_end <= a:
+                s += 1
+                continue
+            b_end = min(seg_end, e)
+            out.append((i, s, a, b_end, i + s))
+            a = b_end
+            s += 1
+    return out
+
+
+def plan(context_lens, num_kv_heads: int, max_blocks_per_seq: int, max_ctas: int,
+         min_pages_per_cta: int, block_size: int = 16) -> dict:
+    """Everything the device planner publishes, as numpy/int values."""
+    pages, bad = segment_pages(context_lens, num_kv_heads, max_blocks_per_seq, block_size)
+    starts = segment_starts(pages)
+    total = int(starts[-1])
+    n = num_ctas(total, max_ctas, min_pages_per_cta)
+    return {
+        "seg_start": starts,
+        "seg_bad": bad,
+        "total_pages": total,
+        "num_ctas": n,
+        "num_segments": int(pages.shape[0]),
+    }
