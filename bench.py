@@ -1,0 +1,548 @@
+"""Benchmark of one paged E5M2-KV GQA decode step on GB300.
+
+A step is one full xqa_decode (planner + split-KV partial + combine) over one
+layer's decode batch. The default workload is 16 sequences with ragged contexts
+drawn uniformly from [16384, 19200] (32 q / 4 kv heads, head_dim 128, 16-token
+pages) — the "B16 ragged 17.8K" workload of the page "[Kernel][SM70] Pipeline
+batched E5M2 XQA decode" (section "Starting bottleneck").
+
+Metric: decode-attention µs/step and KV GB/s (algorithmic KV bytes =
+sum_b ctx_b * Hkv * D * 2 per step, divided by the step time), and the
+partial kernel's fraction of the measured HBM copy bandwidth.
+
+Timing: steps are CUDA-graph replays on one stream, timed with CUDA events;
+the KV cache rotates over several independent pools whose total exceeds the
+129 MB L2 several times, so no step starts with its KV in L2.
+
+``--impl reference`` times the float64 CPU oracle instead, on the same workload,
+each step a bounded sample (one kv head of one sequence over a context prefix).
+
+Under torchrun (N>1) every rank runs its own replica of the workload (weak
+scaling, no collective on the data path); the step time is the maximum over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step and KV GB/s (% of GB300 HBM peak), B16 ragged ~17.8K ctx"
+DEFAULT_WORKLOAD = "b16_ragged_ctx16384_19200"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "partial_kernel_b16_ragged.md")
+KERNEL_SOURCES = ("paged_fp8_kv_gqa_gb300/csrc/partial.cu", "paged_fp8_kv_gqa_gb300/csrc/xqa_device.cuh")
+
+
+# --------------------------------------------------------------------------
+# distributed helpers (host scalars only; no collective on the data path)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend="gloo")
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def reduce_max(dist, x: float) -> float:
+    """Max of a host scalar over ranks (identity without torch.distributed)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# --------------------------------------------------------------------------
+# clocks, peaks, profile traffic
+# --------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows):
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        try:
+            sm.append(float(r[1]))
+            mx.append(float(r[2]))
+        except ValueError:
+            continue
+        for name, val in zip(names, r[5:9]):
+            if val.strip().lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return None
+    sm.sort()
+    return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "samples": len(sm),
+            "reasons": sorted(reasons)}
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per partial-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    src = traffic = None
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if line.startswith("kernel_source_sha256:"):
+            src = line.split(":", 1)[1].strip()
+        elif line.startswith("dram_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    if src != kernel_source_hash() or traffic is None:
+        return None
+    return traffic
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline
+# --------------------------------------------------------------------------
+
+ORACLE_SNIPPET = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from paged_fp8_kv_gqa_gb300 import workloads
+from oracle import attention
+w = workloads.make_workload({name!r})
+budget, t_used, n, times = {budget!r}, 0.0, 0, []
+while t_used < budget or n < 1:
+    t0 = time.perf_counter()
+    attention.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables,
+                                     w.context_lens, w.k_scale, w.v_scale)
+    dt = time.perf_counter() - t0
+    times.append(dt); t_used += dt; n += 1
+times.sort()
+print(json.dumps({{"median_s": times[len(times)//2], "runs": n, "kv_bytes": w.kv_bytes}}))
+"""
+
+
+def cpu_baseline(name: str, budget_s: float = 12.0):
+    """The float64 oracle on the whole workload, single-threaded, in a fresh process."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ORACLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=900)
+    if res.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": "failed: " + res.stderr.strip().splitlines()[-1][:200]}
+    r = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": r["kv_bytes"] / r["median_s"] / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"whole {name} step (all 16 sequences x 4 kv heads), float64 numpy, "
+                      f"1 BLAS thread, median of {r['runs']} runs, {r['median_s']:.2f} s/step"}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_gpu(args, world, rank, local, dist):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_fp8_kv_gqa_gb300 as xqa
+    from paged_fp8_kv_gqa_gb300 import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workloads.make_workload(args.workload)
+    kv_bytes = w.kv_bytes
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q, bt, lens = up(w.q), up(w.block_tables), up(w.context_lens)
+    pools = []
+    k0, v0 = up(w.k_cache), up(w.v_cache)
+    pools.append((k0, v0))
+    for _ in range(args.pools - 1):
+        pools.append((k0.clone(), v0.clone()))
+    shape = xqa.make_shape(q, k0, bt)
+    ws = xqa.alloc_workspace(shape, dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream(device=dev)
+    launches_per_step = 3
+
+    def step(i, ev=None):
+        k, v = pools[i % len(pools)]
+        xqa.xqa_plan(lens, ws, shape, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        xqa.xqa_attend_partial(q, k, v, bt, lens, w.k_scale, w.v_scale, out, ws, shape, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        xqa.xqa_combine(lens, w.v_scale, out, ws, shape, stream)
+
+    # eager warm-up (also sets kernel attributes before any capture)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, min(args.warmup, 50))):
+            step(i)
+    stream.synchronize()
+    assert xqa.xqa_read_status(ws, stream) == xqa.XQA_OK
+
+    # graphs of C steps; per-step partial-kernel events are graph nodes
+    C = max(1, min(args.steps, args.graph_steps))
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(C)]
+    except TypeError:
+        evs = None
+
+    def capture(nsteps, events):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(nsteps):
+                    step(i, events[i] if events else None)
+        return g
+
+    g_main = capture(C, evs)
+    rem = args.steps % C
+    g_tail = capture(rem, None) if rem else None
+    nrep = args.steps // C
+
+    # graph warm-up: at least W steps, and about a second so clocks settle
+    with torch.cuda.stream(stream):
+        t_end = time.time() + args.warm_seconds
+        done = 0
+        while done < args.warmup or time.time() < t_end:
+            g_main.replay()
+            done += C
+            if done % (C * 20) == 0:
+                stream.synchronize()
+    stream.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t0.record(stream)
+    for _ in range(nrep):
+        g_main.replay()
+    if g_tail is not None:
+        g_tail.replay()
+    t1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(dist)
+    clocks = sampler.stop() if sampler is not None else None
+    ms_total = t0.elapsed_time(t1)
+    ms_total_max = reduce_max(dist, ms_total)
+    ms_per_step = ms_total_max / args.steps
+
+    if evs is not None:
+        part_ms = [a.elapsed_time(b) for a, b in evs]
+        timing_note = "CUDA events around every partial launch of the last graph replay"
+    else:  # older torch: time partial-only graph replays
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gp, stream=stream):
+                for i in range(C):
+                    k, v = pools[i % len(pools)]
+                    xqa.xqa_attend_partial(q, k, v, bt, lens, w.k_scale, w.v_scale, out, ws,
+                                           shape, stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        gp.replay()
+        b.record(stream)
+        stream.synchronize()
+        part_ms = [a.elapsed_time(b) / C]
+        timing_note = "partial-only graph replay (no event nodes in this torch)"
+    part_avg_ms = sum(part_ms) / len(part_ms)
+    status = xqa.xqa_read_status(ws, stream)
+
+    # end to end through the public call, host buffers, copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        hq = torch.from_numpy(w.q).pin_memory()
+        hk = torch.from_numpy(w.k_cache).pin_memory()
+        hv = torch.from_numpy(w.v_cache).pin_memory()
+        hbt = torch.from_numpy(w.block_tables).pin_memory()
+        hl = torch.from_numpy(w.context_lens).pin_memory()
+        hout = torch.empty(tuple(w.q.shape), dtype=torch.float16).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k0), torch.empty_like(v0)
+        dbt, dl, dout = torch.empty_like(bt), torch.empty_like(lens), torch.empty_like(out)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hbt, hl))
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for d, h in ((dq, hq), (dk, hk), (dv, hv), (dbt, hbt), (dl, hl)):
+                    d.copy_(h, non_blocking=True)
+                xqa.xqa_decode(dq, dk, dv, dbt, dl, w.k_scale, w.v_scale, out=dout, workspace=ws,
+                               shape=shape, stream=stream)
+                hout.copy_(dout, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        barrier(dist)
+        t_a = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        t_e = reduce_max(dist, time.perf_counter() - t_a)
+        e2e = {"value": aggregate_throughput(kv_bytes * args.e2e_steps, world, t_e) / 1e9,
+               "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps,
+               "us_per_step": t_e / args.e2e_steps * 1e6,
+               "note": "pinned host q, K/V pools, block tables and lengths copied in, "
+                       "output copied out, stream synchronised, every step"}
+
+    if rank != 0:
+        return None
+    peak, peak_kind = hbm_peak()
+    achieved = kv_bytes / (part_avg_ms * 1e-3) / 1e9
+    traffic = profiled_traffic()
+    value = aggregate_throughput(kv_bytes * args.steps, world, ms_total_max * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "us_per_step": ms_per_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 mma / f32 acc (e5m2 kv)",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload,
+            "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size,
+            "total_context_tokens": int(w.context_lens.sum()),
+            "kv_bytes_per_step": kv_bytes,
+            "l2": f"inputs larger than L2: {len(pools)} rotating KV pools of "
+                  f"{2 * w.k_cache.nbytes / 1e6:.0f} MB",
+            "timing": f"CUDA graph replays of {C} steps on one stream, CUDA events",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "pct_of_nominal_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "xqa::partial_kernel",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (STREAM-style copy)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": kv_bytes,
+            "avg_launch_us": part_avg_ms * 1e3,
+            "launch_timing": timing_note,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "device_status": status,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    return line
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# --------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    import numpy as np
+
+    from oracle import attention
+    from paged_fp8_kv_gqa_gb300 import workloads
+
+    if rank != 0:
+        return None
+    w = workloads.make_workload(args.workload)
+    nseg = w.batch * w.num_kv_heads
+    budget = args.reference_seconds
+    # calibrate: one whole segment, then size a context prefix so all steps fit the budget
+    t0 = time.perf_counter()
+    sub = _segment_prefix(w, 0, int(w.context_lens[0]))
+    attention.paged_decode_attention(*sub)
+    per_token = (time.perf_counter() - t0) / int(w.context_lens[0])
+    per_step = budget / max(1, args.steps + args.warmup)
+    tokens = int(max(16, min(int(w.context_lens.min()), per_step / max(per_token, 1e-12))))
+    samples = []
+    for i in range(args.warmup + args.steps):
+        s = i % nseg
+        args_i = _segment_prefix(w, s, tokens)
+        t = time.perf_counter()
+        attention.paged_decode_attention(*args_i)
+        dt = time.perf_counter() - t
+        if i >= args.warmup:
+            samples.append(dt)
+    total = sum(samples)
+    bytes_per_step = tokens * w.head_dim * 2
+    value = bytes_per_step * len(samples) / total / 1e9
+    sample = (f"one kv head of one sequence per step (rotating over the {nseg} (sequence, kv head) "
+              f"pairs), first {tokens} context tokens; float64 numpy oracle")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total / len(samples) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "kv_bytes_per_step": bytes_per_step},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": _threads_note(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def _threads_note():
+    try:
+        return int(os.environ.get("OMP_NUM_THREADS") or 0) or len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def _segment_prefix(w, s, tokens):
+    """Oracle arguments for kv head (s % Hkv) of sequence (s // Hkv) over its first tokens."""
+    import numpy as np
+
+    b, g = divmod(s, w.num_kv_heads)
+    G = w.num_q_heads // w.num_kv_heads
+    n = min(tokens, int(w.context_lens[b]))
+    npg = (n + 15) // 16
+    q = w.q[b:b + 1, g * G:(g + 1) * G]
+    kc = w.k_cache[:, g:g + 1]
+    vc = w.v_cache[:, g:g + 1]
+    bt = w.block_tables[b:b + 1, :npg]
+    lens = np.array([n], np.int32)
+    return q, kc, vc, bt, lens, w.k_scale, w.v_scale
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=("xqa", "reference"), default="xqa")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--pools", type=int, default=4)
+    ap.add_argument("--graph-steps", type=int, default=50)
+    ap.add_argument("--warm-seconds", type=float, default=1.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        dist = init_dist(world)
+        line = run_gpu(args, world, rank, local, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,143 @@
+/*
+ * xqa.h — C ABI of the paged E5M2-KV grouped-query decode-attention library
+ * (libxqa.so, sm_103a).
+ *
+ * One decode step: every sequence b contributes one query token with Hq heads;
+ * its keys and values live in a paged FP8 E5M2 cache; q head h attends over the
+ * ctx_b cached tokens of kv head h / G (G = Hq / Hkv). This is the batched,
+ * long-context XQA decode on an E5M2 KV cache of the page "[Kernel][SM70]
+ * Pipeline batched E5M2 XQA decode" (sections "Purpose" and "Starting
+ * bottleneck"), whose phases (K load + E5M2 conversion, shared-memory
+ * publication, QK, V load + conversion, PV, synchronization; section "Pending
+ * work and gates") are the steps of the partial kernel below. The split-KV
+ * planner -> forward -> merge structure follows the page "[Kernel][WIP] Follow
+ * up FlashNext batch HC fusion and QSA route audit" (section "Test Result").
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers (or managed memory)
+ *     owned by the caller; the library never frees or retains them.
+ *   - The library allocates no memory, keeps no state between calls except a
+ *     per-device "kernel attributes set" flag, reads no environment variables,
+ *     never calls abort/exit and never synchronises except in the
+ *     xqa_read_* helpers, which say so.
+ *   - Work is enqueued on `stream` (a cudaStream_t; 0 = legacy default stream)
+ *     on the current device. A non-OK return means nothing was enqueued unless
+ *     the code is XQA_ERR_LAUNCH.
+ *   - Problems only the device can see (a block id outside [0, NB), a context
+ *     length outside [0, MBS*BS], a pipeline wait that ran out of time) are
+ *     recorded in the status word inside the workspace (read it with
+ *     xqa_read_status); the affected (sequence, kv head) output rows are
+ *     written as NaN, and no out-of-bounds address is ever read.
+ */
+#ifndef XQA_H_
+#define XQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum xqa_status {
+  XQA_OK = 0,
+  XQA_ERR_NULL = 1,        /* a required pointer is NULL */
+  XQA_ERR_SHAPE = 2,       /* unsupported or inconsistent dimensions */
+  XQA_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  XQA_ERR_WORKSPACE = 4,   /* workspace smaller than xqa_workspace_size */
+  XQA_ERR_LAUNCH = 5,      /* a CUDA call or kernel launch failed */
+  XQA_ERR_DEVICE = 6,      /* no usable CUDA device / attribute query failed */
+  /* written by the device into the workspace status word: */
+  XQA_ERR_BAD_BLOCK_ID = 16,    /* block_tables entry outside [0, num_blocks) */
+  XQA_ERR_CTX_TOO_LONG = 17,    /* context length < 0 or > MBS * block_size */
+  XQA_ERR_DEVICE_TIMEOUT = 18   /* a pipeline wait exceeded its time budget */
+} xqa_status_t;
+
+/* Problem dimensions. head_dim must be 128 and block_size 16; Hq must be a
+ * multiple of Hkv with G = Hq / Hkv <= 8. */
+typedef struct xqa_shape {
+  int32_t batch;              /* B: sequences (one query token each), >= 1 */
+  int32_t num_q_heads;        /* Hq */
+  int32_t num_kv_heads;       /* Hkv */
+  int32_t head_dim;           /* D = 128 */
+  int32_t block_size;         /* BS = 16 tokens per page */
+  int32_t max_blocks_per_seq; /* MBS: row length of block_tables */
+  int32_t num_blocks;         /* NB: pages in the K (and V) pool */
+  float sm_scale;             /* softmax scale; <= 0 selects 1/sqrt(D) */
+  int32_t max_ctas;           /* upper bound on split-KV CTAs; 0 = SM count */
+  int32_t min_pages_per_cta;  /* planner lower bound on pages per CTA; 0 = 8 */
+} xqa_shape_t;
+
+/* Bytes of device workspace xqa_decode needs for `shape` on the current
+ * device (depends on the SM count when max_ctas == 0). Host only. */
+xqa_status_t xqa_workspace_size(const xqa_shape_t* shape, size_t* bytes);
+
+/* One decode step of paged GQA attention.
+ *
+ *   q             device, fp16 [B, Hq, D], contiguous, 16-byte aligned
+ *   k_cache       device, E5M2 bytes [NB, Hkv, BS, D] (one (page, kv head)
+ *                 slice is BS*D = 2048 contiguous bytes), 16-byte aligned
+ *   v_cache       device, same layout as k_cache
+ *   block_tables  device, int32 [B, MBS]; entry j of row b is the physical page
+ *                 of tokens [16j, 16j+16) of sequence b; entries at or past
+ *                 ceil(ctx_b / 16) are never read
+ *   context_lens  device, int32 [B]; 0 <= ctx_b <= MBS*BS (0 gives a zero row)
+ *   k_scale       per-tensor K scale (the key value is k_scale * E5M2(code))
+ *   v_scale       per-tensor V scale
+ *   out           device, fp16 [B, Hq, D], contiguous, 16-byte aligned
+ *   workspace     device, >= xqa_workspace_size bytes, 256-byte aligned; holds
+ *                 the plan, the split partials and the status word; contents
+ *                 need no initialisation and are overwritten every call
+ *
+ * out[b, h, :] = sum_t softmax_t(sm_scale * <q[b,h], k_t>) * v_t over the
+ * ctx_b tokens of kv head h / G, rounded to fp16 (round to nearest even).
+ * Three kernels are enqueued: planner, split-KV partial, log-sum-exp combine.
+ * No host synchronisation; the call may be captured into a CUDA graph.
+ * Concurrent calls must not share a workspace. */
+xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens,
+                        float k_scale, float v_scale, void* out, const xqa_shape_t* shape,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* The three stages of xqa_decode, exposed separately so they can be timed one
+ * by one. Called in this order with the same arguments they are exactly
+ * xqa_decode. */
+xqa_status_t xqa_plan(const int32_t* context_lens, const xqa_shape_t* shape, void* workspace,
+                      size_t workspace_bytes, void* stream);
+xqa_status_t xqa_attend_partial(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float k_scale, float v_scale, void* out,
+                                const xqa_shape_t* shape, void* workspace,
+                                size_t workspace_bytes, void* stream);
+xqa_status_t xqa_combine(const int32_t* context_lens, float v_scale, void* out,
+                         const xqa_shape_t* shape, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Exact E5M2 dequantisation (the "E5M2 conversion" phase on its own):
+ *   out_fp16_bits[i] = (uint16_t)in[i] << 8        (the fp16 pattern, exact)
+ *   out_f32[i]       = (float)fp16(in[i]) * scale  (optional; NULL to skip)
+ * in, out_fp16_bits, out_f32: device pointers, n elements each; any
+ * alignment. */
+xqa_status_t xqa_dequant_e5m2(const uint8_t* in, size_t n, float scale, uint16_t* out_fp16_bits,
+                              float* out_f32, void* stream);
+
+/* Copies the workspace status word to *device_status (an xqa_status_t value:
+ * XQA_OK or one of the device-reported codes). Synchronises `stream`. */
+xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void* stream);
+
+/* Copies the planner's output to host memory. Synchronises `stream`.
+ *   header[4]          = {status, num_ctas, total_pages, num_segments}
+ *   seg_start[B*Hkv+1] = exclusive prefix sum of pages per (sequence, kv head)
+ *   seg_bad[B*Hkv]     = 1 where the segment's context length is invalid or a
+ *                        bad block id was met, else 0 (may be NULL) */
+xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int32_t* header,
+                           int32_t* seg_start, int32_t* seg_bad, void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* xqa_status_string(xqa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XQA_H_ */

@@ -1,0 +1,78 @@
+// combine.cu — log-sum-exp merge of the split-KV partial results.
+//
+// One CTA per (sequence, kv head) segment. Segments processed whole by one
+// partial CTA were already written by it; this kernel writes zero rows for
+// empty segments (context length 0), NaN rows for bad segments and, for a
+// segment split over CTAs i_lo..i_hi, merges their pieces (slot i + s):
+//   M = max_i m_i,  w_i = 2^(m_i - M),  L = sum_i w_i l_i,
+//   out = fp16(sum_i w_i o_i * (v_scale / L))    (round to nearest even).
+// This is the "merge" phase of the planner -> forward -> merge split-KV
+// structure on the page "[Kernel][WIP] Follow up FlashNext batch HC fusion and
+// QSA route audit" (section "Test Result").
+#include <math.h>
+
+#include "xqa_device.cuh"
+#include "xqa_launch.h"
+
+namespace xqa {
+
+__device__ __forceinline__ void store_half4(__half* dst, float a, float b, float c, float d) {
+  uint2 v;
+  v.x = pack_half2(a, b);
+  v.y = pack_half2(c, d);
+  *reinterpret_cast<uint2*>(dst) = v;
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
+  const int s = blockIdx.x;
+  const int h = threadIdx.x >> 5;
+  const int dq = (threadIdx.x & 31) * 4;
+  if (h >= p.group) return;
+  const int n = p.header[1];
+  const long long total = p.header[2];
+  const int sb = p.seg_start[s], se = p.seg_start[s + 1];
+  const bool bad = p.seg_bad[s] != 0;
+  const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+  __half* o = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim + dq;
+  if (sb == se) {
+    const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
+    store_half4(o, v, v, v, v);
+    return;
+  }
+  const int ilo = (int)(((long long)(sb + 1) * n - 1) / total);
+  const int ihi = (int)(((long long)se * n - 1) / total);
+  if (ilo == ihi) return;  // written whole by its partial CTA
+  if (bad) {
+    const float v = __int_as_float(0x7fc00000);
+    store_half4(o, v, v, v, v);
+    return;
+  }
+  float M = -INFINITY;
+  for (int i = ilo; i <= ihi; ++i) {
+    const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
+    M = fmaxf(M, slot[kMaxGroup * kHeadDim + h]);
+  }
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = ilo; i <= ihi; ++i) {
+    const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
+    const float mi = slot[kMaxGroup * kHeadDim + h];
+    const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
+    L += w * slot[kMaxGroup * kHeadDim + kMaxGroup + h];
+    const float4 v = *reinterpret_cast<const float4*>(slot + h * kHeadDim + dq);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
+  const float r = p.v_scale / L;
+  store_half4(o, acc.x * r, acc.y * r, acc.z * r, acc.w * r);
+}
+
+cudaError_t launch_combine(const CombineParams& p, int num_segments, cudaStream_t stream) {
+  if (num_segments <= 0) return cudaSuccess;
+  combine_kernel<<<num_segments, kCombineThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace xqa

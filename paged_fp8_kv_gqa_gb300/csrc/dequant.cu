@@ -1,0 +1,63 @@
+// dequant.cu — the exact E5M2 -> fp16 conversion on its own, for testing.
+//
+// Each thread converts one 8-byte group with the same byte-permutation helpers
+// the attention kernel uses: even groups take the "adjacent codes of one word"
+// route used for K, odd groups the "same byte of two words" route used for V,
+// so a test over all 256 codes at both parities checks both routes bit for bit.
+// This is the "E5M2 conversion" phase named on the page "[Kernel][SM70]
+// Pipeline batched E5M2 XQA decode" (section "Pending work and gates").
+#include "xqa_device.cuh"
+#include "xqa_launch.h"
+
+namespace xqa {
+
+__global__ void dequant_kernel(const uint8_t* __restrict__ in, size_t n, float scale,
+                               uint16_t* __restrict__ out16, float* __restrict__ out32) {
+  const size_t ngroups = (n + 7) / 8;
+  for (size_t grp = (size_t)blockIdx.x * blockDim.x + threadIdx.x; grp < ngroups;
+       grp += (size_t)gridDim.x * blockDim.x) {
+    const size_t base = grp * 8;
+    uint32_t x = 0, y = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (base + k < n) x |= (uint32_t)in[base + k] << (8 * k);
+      if (base + 4 + k < n) y |= (uint32_t)in[base + 4 + k] << (8 * k);
+    }
+    uint16_t h[8];
+    if ((grp & 1) == 0) {
+      const uint32_t r[4] = {e5m2x2_lo(x), e5m2x2_hi(x), e5m2x2_lo(y), e5m2x2_hi(y)};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        h[2 * k] = (uint16_t)(r[k] & 0xffffu);
+        h[2 * k + 1] = (uint16_t)(r[k] >> 16);
+      }
+    } else {
+      const uint32_t i01 = interleave01(x, y), i23 = interleave23(x, y);
+      const uint32_t r[4] = {pair_even(i01), pair_odd(i01), pair_even(i23), pair_odd(i23)};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // r[k] = {x_k, y_k}
+        h[k] = (uint16_t)(r[k] & 0xffffu);
+        h[4 + k] = (uint16_t)(r[k] >> 16);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (base + k < n) {
+        out16[base + k] = h[k];
+        if (out32) out32[base + k] = __half2float(__ushort_as_half(h[k])) * scale;
+      }
+    }
+  }
+}
+
+cudaError_t launch_dequant(const uint8_t* in, size_t n, float scale, uint16_t* out16,
+                           float* out32, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const size_t ngroups = (n + 7) / 8;
+  size_t blocks = (ngroups + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  dequant_kernel<<<(unsigned)blocks, 256, 0, stream>>>(in, n, scale, out16, out32);
+  return cudaGetLastError();
+}
+
+}  // namespace xqa

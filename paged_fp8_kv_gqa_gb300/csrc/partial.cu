@@ -1,0 +1,432 @@
+// partial.cu — the split-KV partial attention kernel (the hot loop).
+//
+// One persistent CTA per planner share of the flattened (sequence, kv head,
+// page) order. Its phases are the ones profiled on the page "[Kernel][SM70]
+// Pipeline batched E5M2 XQA decode" (section "Pending work and gates"): K load +
+// E5M2 conversion, shared-memory publication, QK, V load + conversion, PV and
+// synchronization. That page's starting kernel was memory-latency bound
+// (long-scoreboard stalls at low occupancy, section "Starting bottleneck"); on
+// sm_103a this kernel keeps up to kStages pages in flight per SM instead:
+//
+//  * producer warp: walks the block table (bounds-checked) and issues, per
+//    page, two 2-D TMA loads (K slice and V slice, 2048 B each, 128-byte
+//    swizzle) into a kStages-deep shared-memory ring; mbarrier full/empty
+//    pairs publish the stages;
+//  * 8 consumer warps: warp w takes ring stages w, w+8, ...; per 16-token page
+//      - reads K and V with conflict-free 16-byte shared loads,
+//      - dequantises exactly (fp16 pattern = code << 8, a byte permutation),
+//      - S^T[16 tok x 8 heads] = K * Q^T with 8 m16n8k16 MMAs (fp32 accumulate),
+//      - online softmax in the log2 domain (k_scale and sm_scale folded into
+//        one fp32 logit scale; the running max only moves when a logit exceeds
+//        it by more than 8, so most pages skip the rescale),
+//      - P^T to the B-operand layout with two movmatrix transposes,
+//      - O^T[128 x 8] += V^T * P^T with 8 MMAs plus one MMA against ones for the
+//        row sums l (so l sums exactly the fp16 P used for O);
+//  * at the end of every segment the 8 warps' (m, l, O) are merged in shared
+//    memory; a segment owned whole by this CTA is normalised and written as fp16
+//    (out = O * (v_scale / l)); otherwise the piece goes to partial slot i + s
+//    for the combine kernel.
+//
+// Contraction-index permutation: the MMA result does not depend on how the
+// contraction index is laid out, as long as both operands use the same layout.
+// QK lane (g, c) owns dims [32c, 32c+32) of its two token rows; PV lane (g, c)
+// owns dims [16g, 16g+16) of tokens {2c, 2c+1, 2c+8, 2c+9}. Both read 16 B per
+// shared load, and the TMA 128-byte swizzle (chunk ^= row & 7) makes every
+// 8-lane phase hit 8 distinct 16-byte chunks.
+#include <math.h>
+
+#include "xqa_device.cuh"
+#include "xqa_launch.h"
+
+namespace xqa {
+
+namespace {
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kOnesHalf2 = 0x3C003C00u;
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ int consumer_bar_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "n"(kConsumerWarps * 32)
+      : "memory");
+  return r;
+}
+
+// Largest s in [0, nseg) with seg_start[s] <= page (seg_start[nseg] > page).
+__device__ __forceinline__ int find_segment(const int32_t* seg_start, int nseg, int page) {
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&seg_start[mid]) <= page) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct WarpState {
+  float o[8][4];  // O^T tiles: [tile i][c-frag]; rows d = 16g + 2i (+1), cols heads 2c (+1)
+  float l[4];     // row sums per head (cols 2c, 2c+1), replicated over rows
+  float m0, m1;   // running max (log2 domain) of heads 2c and 2c+1
+};
+
+__device__ __forceinline__ void reset_state(WarpState& st) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st.o[i][k] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) st.l[k] = 0.f;
+  st.m0 = -INFINITY;
+  st.m1 = -INFINITY;
+}
+
+// One 16-token page of one kv head: QK, online softmax, PV.
+__device__ __forceinline__ void process_page(WarpState& st, const uint8_t* ks, const uint8_t* vs,
+                                             const uint32_t (&qf)[16], int nvalid, float scale_log2,
+                                             int g, int c, uint64_t* empty_bar, int lane) {
+  // ---- K and V shared loads (swizzled 16-byte chunks) ----
+  const int kc0 = ((2 * c) ^ g) << 4, kc1 = ((2 * c + 1) ^ g) << 4;
+  const uint4 ka0 = lds128(ks + g * 128 + kc0);
+  const uint4 ka1 = lds128(ks + g * 128 + kc1);
+  const uint4 kb0 = lds128(ks + (g + 8) * 128 + kc0);
+  const uint4 kb1 = lds128(ks + (g + 8) * 128 + kc1);
+  const int ve = (g ^ (2 * c)) << 4, vo = (g ^ (2 * c + 1)) << 4;
+  uint4 vx = lds128(vs + (2 * c) * 128 + ve);
+  uint4 vy = lds128(vs + (2 * c + 1) * 128 + vo);
+  uint4 vz = lds128(vs + (2 * c + 8) * 128 + ve);
+  uint4 vw = lds128(vs + (2 * c + 9) * 128 + vo);
+  if (nvalid < kBlockSize) {  // zero V rows past the context (0 * NaN would poison O)
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    if (2 * c >= nvalid) vx = z;
+    if (2 * c + 1 >= nvalid) vy = z;
+    if (2 * c + 8 >= nvalid) vz = z;
+    if (2 * c + 9 >= nvalid) vw = z;
+  }
+
+  // ---- S^T = K * Q^T : rows tokens (g, g+8), cols heads (2c, 2c+1) ----
+  const uint32_t kr0[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+  const uint32_t kr1[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    mma_16816(s, e5m2x2_lo(kr0[j]), e5m2x2_lo(kr1[j]), e5m2x2_hi(kr0[j]), e5m2x2_hi(kr1[j]),
+              qf[2 * j], qf[2 * j + 1]);
+  }
+
+  // ---- online softmax (log2 domain) ----
+  float t0 = s[0] * scale_log2, t1 = s[1] * scale_log2;
+  float t2 = s[2] * scale_log2, t3 = s[3] * scale_log2;
+  if (nvalid < kBlockSize) {
+    if (g >= nvalid) t0 = t1 = -INFINITY;
+    if (g + 8 >= nvalid) t2 = t3 = -INFINITY;
+  }
+  float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+  const bool need = (mx0 > st.m0 + kRescaleThreshold) || (mx1 > st.m1 + kRescaleThreshold);
+  if (__any_sync(kFull, need)) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+    }
+    const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
+    const float a0 = ex2(st.m0 - n0), a1 = ex2(st.m1 - n1);
+    st.m0 = n0;
+    st.m1 = n1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      st.o[i][0] *= a0;
+      st.o[i][2] *= a0;
+      st.o[i][1] *= a1;
+      st.o[i][3] *= a1;
+    }
+    st.l[0] *= a0;
+    st.l[2] *= a0;
+    st.l[1] *= a1;
+    st.l[3] *= a1;
+  }
+  const float p0 = ex2(t0 - st.m0), p1 = ex2(t1 - st.m1);
+  const float p2 = ex2(t2 - st.m0), p3 = ex2(t3 - st.m1);
+  // P^T B-fragments: lane (g, c) gets P[tokens 2c, 2c+1 | 2c+8, 2c+9][head g]
+  const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));
+  const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));
+
+  // ---- O^T += V^T * P^T ----
+  const uint32_t X[4] = {vx.x, vx.y, vx.z, vx.w}, Y[4] = {vy.x, vy.y, vy.z, vy.w};
+  const uint32_t Z[4] = {vz.x, vz.y, vz.z, vz.w}, W[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint32_t xy01 = interleave01(X[u], Y[u]), xy23 = interleave23(X[u], Y[u]);
+    const uint32_t zw01 = interleave01(Z[u], W[u]), zw23 = interleave23(Z[u], W[u]);
+    mma_16816(st.o[2 * u], pair_even(xy01), pair_odd(xy01), pair_even(zw01), pair_odd(zw01), pb0,
+              pb1);
+    mma_16816(st.o[2 * u + 1], pair_even(xy23), pair_odd(xy23), pair_even(zw23), pair_odd(zw23),
+              pb0, pb1);
+  }
+  // every shared byte of this stage is in registers and consumed: release it
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+  mma_16816(st.l, kOnesHalf2, kOnesHalf2, kOnesHalf2, kOnesHalf2, pb0, pb1);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const PartialParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ int stage_bad[kStages];
+  __shared__ int abort_flag;
+
+  const int n = p.header[1];
+  const int cta = blockIdx.x;
+  if (cta >= n) return;
+  const long long total = p.header[2];
+  const int cbeg = (int)(((long long)cta * total) / n);
+  const int cend = (int)(((long long)(cta + 1) * total) / n);
+  const int npages = cend - cbeg;
+  const int nseg = p.batch * p.num_kv_heads;
+
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* scratch = reinterpret_cast<float*>(stages + kStages * kStageBytes);
+  float* scr_m = scratch + kScratchFloats;
+  float* scr_l = scr_m + kConsumerWarps * kMaxGroup;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int s_first = find_segment(p.seg_start, nseg, cbeg);
+  volatile int* abort = &abort_flag;
+
+  if (warp == kConsumerWarps) {
+    // ======================= producer warp =======================
+    const uint64_t policy = l2_evict_first_policy();
+    int s_cur = s_first;
+    bool aborted = false;
+    int issued = 0;
+    for (int base = 0; base < npages && !aborted; base += 32) {
+      const int qi = base + lane;
+      const int pg = cbeg + qi;
+      int s = s_cur, y = 0, bad = 0;
+      if (qi < npages) {
+        while (__ldg(&p.seg_start[s + 1]) <= pg) ++s;
+        const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+        const int j = pg - __ldg(&p.seg_start[s]);
+        const int id = __ldg(&p.block_tables[(size_t)b * p.max_blocks_per_seq + j]);
+        bad = (id < 0 || id >= p.num_blocks) ? 1 : 0;
+        y = bad ? 0 : (id * p.num_kv_heads + kvh) * kBlockSize;
+      }
+      const int cnt = min(32, npages - base);
+      for (int l = 0; l < cnt; ++l) {
+        const int qq = base + l;
+        const int slot = qq % kStages, use = qq / kStages;
+        const int yl = __shfl_sync(kFull, y, l);
+        const int badl = __shfl_sync(kFull, bad, l);
+        const int sl = __shfl_sync(kFull, s, l);
+        if (use > 0) {
+          const bool ok = mbar_wait_bounded(&empty_bar[slot], (use - 1) & 1, abort);
+          if (!__all_sync(kFull, ok)) {  // warp-uniform outcome
+            aborted = true;
+            break;
+          }
+        }
+        if (lane == 0) {
+          uint8_t* st = stages + slot * kStageBytes;
+          stage_bad[slot] = badl;
+          if (badl) {
+            atomicOr(&p.seg_bad[sl], 1);
+            record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
+            mbar_arrive(&full_bar[slot]);
+          } else {
+            mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
+            tma_load_2d(st, &tm_k, &full_bar[slot], 0, yl, policy);
+            tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, yl, policy);
+          }
+        }
+        __syncwarp();
+        issued = qq + 1;
+      }
+      s_cur = __shfl_sync(kFull, s, cnt - 1);
+    }
+    if (aborted && lane == 0) {
+      *abort = 1;
+      record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
+    }
+    // Drain: every copy this warp issued must land before the warp exits, so no
+    // bulk copy can outlive the CTA's shared memory even if consumers gave up.
+    // The last kStages issued stages are the only ones that can be in flight.
+    {
+      int never = 0;
+      volatile int* no_abort = &never;
+      for (int qq = issued > kStages ? issued - kStages : 0; qq < issued; ++qq) {
+        const bool ok = mbar_wait_bounded(&full_bar[qq % kStages], (qq / kStages) & 1, no_abort);
+        if (!__all_sync(kFull, ok)) {
+          if (lane == 0) record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ======================= consumer warps =======================
+  const int g = lane >> 2, c = lane & 3;
+  WarpState st;
+  int s = s_first;
+  int q0 = 0;
+  while (q0 < npages) {
+    while (__ldg(&p.seg_start[s + 1]) <= cbeg + q0) ++s;
+    const int sb = __ldg(&p.seg_start[s]), se = __ldg(&p.seg_start[s + 1]);
+    const int qe = min(se, cend) - cbeg;
+    const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+    const int ctx = __ldg(&p.context_lens[b]);
+    const bool whole = (sb >= cbeg) && (se <= cend);
+
+    uint32_t qf[16];
+    if (g < p.group) {
+      const uint4* qp = reinterpret_cast<const uint4*>(
+          p.q + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + g) * kHeadDim + 32 * c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldg(qp + i);
+        qf[4 * i] = v.x;
+        qf[4 * i + 1] = v.y;
+        qf[4 * i + 2] = v.z;
+        qf[4 * i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) qf[i] = 0u;
+    }
+    reset_state(st);
+    int poisoned = 0;
+
+    for (int q = q0 + ((warp - q0 % kConsumerWarps) + kConsumerWarps) % kConsumerWarps; q < qe;
+         q += kConsumerWarps) {
+      const int slot = q % kStages;
+      const bool ready = mbar_wait_bounded(&full_bar[slot], (q / kStages) & 1, abort);
+      if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
+        poisoned = 1;
+        if (lane == 0) {
+          *abort = 1;
+          record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
+        }
+        continue;
+      }
+      if (stage_bad[slot]) {
+        poisoned = 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+        continue;
+      }
+      const int j = cbeg + q - sb;
+      const int nvalid = min(kBlockSize, ctx - j * kBlockSize);
+      const uint8_t* stg = stages + slot * kStageBytes;
+      process_page(st, stg, stg + kPageBytes, qf, nvalid, p.scale_log2, g, c, &empty_bar[slot],
+                   lane);
+    }
+
+    // ---- merge the 8 warps' states for this segment ----
+    {
+      float* my = scratch + warp * kMaxGroup * kScratchStride;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int d0 = 16 * g + 2 * i;
+        my[(2 * c) * kScratchStride + d0] = st.o[i][0];
+        my[(2 * c + 1) * kScratchStride + d0] = st.o[i][1];
+        my[(2 * c) * kScratchStride + d0 + 1] = st.o[i][2];
+        my[(2 * c + 1) * kScratchStride + d0 + 1] = st.o[i][3];
+      }
+      if (g == 0) {
+        scr_m[warp * kMaxGroup + 2 * c] = st.m0;
+        scr_m[warp * kMaxGroup + 2 * c + 1] = st.m1;
+        scr_l[warp * kMaxGroup + 2 * c] = st.l[0];
+        scr_l[warp * kMaxGroup + 2 * c + 1] = st.l[1];
+      }
+    }
+    const int any_poison = consumer_bar_or(poisoned);
+    {
+      const int h = tid >> 5;          // 0..7
+      const int dq = (tid & 31) * 4;   // 0..124
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, scr_m[w * kMaxGroup + h]);
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = scr_m[w * kMaxGroup + h];
+        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        L += sc * scr_l[w * kMaxGroup + h];
+        const float4 v =
+            *reinterpret_cast<const float4*>(scratch + (w * kMaxGroup + h) * kScratchStride + dq);
+        acc.x += sc * v.x;
+        acc.y += sc * v.y;
+        acc.z += sc * v.z;
+        acc.w += sc * v.w;
+      }
+      if (h < p.group) {
+        if (whole) {
+          __half* o = p.out +
+                      ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim + dq;
+          float r = p.v_scale / L;
+          uint2 v;
+          if (any_poison) {
+            const float nan = __int_as_float(0x7fc00000);
+            v.x = pack_half2(nan, nan);
+            v.y = v.x;
+          } else {
+            v.x = pack_half2(acc.x * r, acc.y * r);
+            v.y = pack_half2(acc.z * r, acc.w * r);
+          }
+          *reinterpret_cast<uint2*>(o) = v;
+        } else {
+          float* slotp = p.partials + (size_t)(cta + s) * kSlotFloats;
+          *reinterpret_cast<float4*>(slotp + h * kHeadDim + dq) = acc;
+          if (dq == 0) {
+            slotp[kMaxGroup * kHeadDim + h] = M;
+            slotp[kMaxGroup * kHeadDim + kMaxGroup + h] = L;
+          }
+          if (any_poison && tid == 0) atomicOr(&p.seg_bad[s], 1);
+        }
+      }
+    }
+    consumer_bar();  // scratch is reused by the next segment
+    q0 = qe;
+    ++s;
+  }
+}
+
+cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                           const PartialParams& p, int n_max, cudaStream_t stream) {
+  partial_kernel<<<n_max, kThreads, kPartialSmem, stream>>>(tm_k, tm_v, p);
+  return cudaGetLastError();
+}
+
+cudaError_t set_partial_attributes() {
+  return cudaFuncSetAttribute(partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kPartialSmem);
+}
+
+}  // namespace xqa

@@ -1,0 +1,90 @@
+// plan.cu — the split-KV planner (one CTA).
+//
+// Reads context_lens[B] and publishes, in the workspace, the pages of every
+// (sequence, kv head) segment as an exclusive prefix sum, the bad-segment
+// flags, the total page count and the number of partial-kernel CTAs. CTA i of
+// the partial kernel then owns flattened pages [floor(i*P/n), floor((i+1)*P/n)):
+// every CTA gets the same share whatever the length mix, long sequences are
+// split across CTAs and short ones share a CTA. This answers the two failure
+// modes recorded on the page "[Kernel][WIP] Follow up FlashNext batch HC fusion
+// and QSA route audit" (section "Test Result"): a capacity-sized grid with
+// empty CTAs on short contexts, and fixed grids that regress long ones. The
+// plan is computed on the device so the decode step needs no host sync.
+#include "xqa_device.cuh"
+#include "xqa_launch.h"
+
+namespace xqa {
+
+__device__ __forceinline__ int warp_inclusive_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int u = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += u;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ context_lens,
+                                                            int batch, int num_kv_heads,
+                                                            int max_blocks_per_seq, int n_max,
+                                                            int min_pages, int32_t* ws) {
+  const int nseg = batch * num_kv_heads;
+  int32_t* header = ws;
+  int32_t* seg_start = ws + 4;
+  int32_t* seg_bad = seg_start + nseg + 1;
+  __shared__ int warp_total[kPlanThreads / 32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    header[0] = XQA_OK;
+    carry = 0;
+  }
+  __syncthreads();
+  const long long max_ctx = (long long)max_blocks_per_seq * kBlockSize;
+  for (int base = 0; base < nseg; base += kPlanThreads) {
+    const int s = base + tid;
+    int pages = 0;
+    if (s < nseg) {
+      const int ctx = context_lens[s / num_kv_heads];
+      const bool bad = ctx < 0 || (long long)ctx > max_ctx;
+      if (bad) record_status(&header[0], XQA_ERR_CTX_TOO_LONG);
+      pages = bad ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
+      seg_bad[s] = bad ? 1 : 0;
+    }
+    const int incl = warp_inclusive_scan(pages);
+    if (lane == 31) warp_total[warp] = incl;
+    __syncthreads();
+    if (warp == 0) warp_total[lane] = warp_inclusive_scan(warp_total[lane]);
+    __syncthreads();
+    const int excl = carry + incl - pages + (warp > 0 ? warp_total[warp - 1] : 0);
+    if (s < nseg) seg_start[s] = excl;
+    __syncthreads();
+    if (tid == kPlanThreads - 1) carry = excl + pages;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const int total = carry;
+    seg_start[nseg] = total;
+    header[2] = total;
+    header[3] = nseg;
+    int n = 0;
+    if (total > 0) {
+      const int want = (total + min_pages - 1) / min_pages;
+      n = want < 1 ? 1 : want;
+      n = n < n_max ? n : n_max;
+    }
+    header[1] = n;
+  }
+}
+
+cudaError_t launch_plan(const int32_t* context_lens, int batch, int num_kv_heads,
+                        int max_blocks_per_seq, int n_max, int min_pages_per_cta,
+                        int32_t* workspace, cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(context_lens, batch, num_kv_heads,
+                                              max_blocks_per_seq, n_max, min_pages_per_cta,
+                                              workspace);
+  return cudaGetLastError();
+}
+
+}  // namespace xqa

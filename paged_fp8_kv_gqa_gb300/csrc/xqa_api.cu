@@ -1,0 +1,281 @@
+// xqa_api.cu — the C ABI of libxqa: argument validation, TMA descriptors and
+// the planner -> partial -> combine launches. See include/xqa.h for the
+// contract of every entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "xqa.h"
+#include "xqa_device.cuh"
+#include "xqa_launch.h"
+
+namespace xqa {
+cudaError_t set_partial_attributes();
+}
+
+namespace {
+
+using xqa::kBlockSize;
+using xqa::kHeadDim;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_attrs_set[kMaxDevices];
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
+
+struct Resolved {
+  int batch, hq, hkv, group, mbs, nb;
+  int nseg, n_max, min_pages;
+  float sm_scale;
+  xqa::WsLayout ws;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
+  if (!s) return XQA_ERR_NULL;
+  if (s->head_dim != kHeadDim || s->block_size != kBlockSize) return XQA_ERR_SHAPE;
+  if (s->batch < 1 || s->num_kv_heads < 1 || s->num_q_heads < 1) return XQA_ERR_SHAPE;
+  if (s->num_q_heads % s->num_kv_heads != 0) return XQA_ERR_SHAPE;
+  const int group = s->num_q_heads / s->num_kv_heads;
+  if (group > xqa::kMaxGroup) return XQA_ERR_SHAPE;
+  if (s->max_blocks_per_seq < 1 || s->num_blocks < 1) return XQA_ERR_SHAPE;
+  if (s->max_ctas < 0 || s->min_pages_per_cta < 0) return XQA_ERR_SHAPE;
+  // int32 index arithmetic on the device: pool rows, total pages, segments
+  const long long pool_rows = (long long)s->num_blocks * s->num_kv_heads * kBlockSize;
+  const long long max_pages = (long long)s->batch * s->num_kv_heads * s->max_blocks_per_seq;
+  if (pool_rows >= (1ll << 31) || max_pages >= (1ll << 31)) return XQA_ERR_SHAPE;
+  if ((long long)s->batch * s->num_q_heads >= (1ll << 31) / kHeadDim) return XQA_ERR_SHAPE;
+  r->batch = s->batch;
+  r->hq = s->num_q_heads;
+  r->hkv = s->num_kv_heads;
+  r->group = group;
+  r->mbs = s->max_blocks_per_seq;
+  r->nb = s->num_blocks;
+  r->nseg = s->batch * s->num_kv_heads;
+  r->sm_scale = s->sm_scale > 0.f ? s->sm_scale : (float)(1.0 / sqrt((double)kHeadDim));
+  r->min_pages = s->min_pages_per_cta > 0 ? s->min_pages_per_cta : xqa::kDefaultMinPagesPerCta;
+  if (s->max_ctas > 0) {
+    r->n_max = s->max_ctas;
+  } else {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return XQA_ERR_DEVICE;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms < 1)
+      return XQA_ERR_DEVICE;
+    r->n_max = sms;
+  }
+  if (r->n_max > 65535) r->n_max = 65535;
+  r->ws = xqa::ws_layout(r->nseg, r->n_max);
+  return XQA_OK;
+}
+
+xqa_status_t check_workspace(const Resolved& r, const void* ws, size_t bytes) {
+  if (!ws) return XQA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return XQA_ERR_ALIGN;
+  if (bytes < r.ws.total) return XQA_ERR_WORKSPACE;
+  return XQA_OK;
+}
+
+xqa_status_t ensure_device_setup() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return XQA_ERR_DEVICE;
+  if (dev < 0 || dev >= kMaxDevices) return XQA_ERR_DEVICE;
+  if (g_attrs_set[dev].load(std::memory_order_acquire) == 0) {
+    if (xqa::set_partial_attributes() != cudaSuccess) return XQA_ERR_LAUNCH;
+    g_attrs_set[dev].store(1, std::memory_order_release);
+  }
+  if (g_encode.load(std::memory_order_acquire) == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return XQA_ERR_DEVICE;
+    g_encode.store(reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn),
+                   std::memory_order_release);
+  }
+  return XQA_OK;
+}
+
+// 2-D view of a [NB, Hkv, BS, D] byte pool: x = D (128 B rows), y = NB*Hkv*BS;
+// box = one (page, kv head) slice of BS x D bytes, 128-byte swizzle.
+xqa_status_t encode_pool_map(CUtensorMap* map, const uint8_t* pool, const Resolved& r) {
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)r.nb * r.hkv * kBlockSize};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+  cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)kBlockSize};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult res = g_encode.load(std::memory_order_acquire)(
+      map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(pool), dims, strides, box,
+      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS ? XQA_OK : XQA_ERR_LAUNCH;
+}
+
+int32_t* ws_i32(void* ws) { return reinterpret_cast<int32_t*>(ws); }
+
+}  // namespace
+
+extern "C" {
+
+xqa_status_t xqa_workspace_size(const xqa_shape_t* shape, size_t* bytes) {
+  if (!bytes) return XQA_ERR_NULL;
+  Resolved r;
+  xqa_status_t st = resolve(shape, &r);
+  if (st != XQA_OK) return st;
+  *bytes = r.ws.total;
+  return XQA_OK;
+}
+
+xqa_status_t xqa_plan(const int32_t* context_lens, const xqa_shape_t* shape, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!context_lens) return XQA_ERR_NULL;
+  Resolved r;
+  xqa_status_t st = resolve(shape, &r);
+  if (st != XQA_OK) return st;
+  if ((st = check_workspace(r, workspace, workspace_bytes)) != XQA_OK) return st;
+  cudaError_t e = xqa::launch_plan(context_lens, r.batch, r.hkv, r.mbs, r.n_max, r.min_pages,
+                                   ws_i32(workspace), (cudaStream_t)stream);
+  return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
+}
+
+xqa_status_t xqa_attend_partial(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float k_scale, float v_scale, void* out,
+                                const xqa_shape_t* shape, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return XQA_ERR_NULL;
+  Resolved r;
+  xqa_status_t st = resolve(shape, &r);
+  if (st != XQA_OK) return st;
+  if ((st = check_workspace(r, workspace, workspace_bytes)) != XQA_OK) return st;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return XQA_ERR_ALIGN;
+  if ((st = ensure_device_setup()) != XQA_OK) return st;
+  alignas(64) CUtensorMap tm_k, tm_v;
+  if ((st = encode_pool_map(&tm_k, k_cache, r)) != XQA_OK) return st;
+  if ((st = encode_pool_map(&tm_v, v_cache, r)) != XQA_OK) return st;
+  uint8_t* base = reinterpret_cast<uint8_t*>(workspace);
+  xqa::PartialParams p;
+  p.q = reinterpret_cast<const __half*>(q);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = reinterpret_cast<__half*>(out);
+  p.header = ws_i32(workspace);
+  p.seg_start = reinterpret_cast<const int32_t*>(base + r.ws.seg_start_off);
+  p.seg_bad = reinterpret_cast<int32_t*>(base + r.ws.seg_bad_off);
+  p.partials = reinterpret_cast<float*>(base + r.ws.partials_off);
+  p.batch = r.batch;
+  p.num_q_heads = r.hq;
+  p.num_kv_heads = r.hkv;
+  p.group = r.group;
+  p.max_blocks_per_seq = r.mbs;
+  p.num_blocks = r.nb;
+  p.scale_log2 = (float)((double)r.sm_scale * (double)k_scale * 1.4426950408889634);
+  p.v_scale = v_scale;
+  cudaError_t e = xqa::launch_partial(tm_k, tm_v, p, r.n_max, (cudaStream_t)stream);
+  return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
+}
+
+xqa_status_t xqa_combine(const int32_t* context_lens, float v_scale, void* out,
+                         const xqa_shape_t* shape, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (!context_lens || !out) return XQA_ERR_NULL;
+  Resolved r;
+  xqa_status_t st = resolve(shape, &r);
+  if (st != XQA_OK) return st;
+  if ((st = check_workspace(r, workspace, workspace_bytes)) != XQA_OK) return st;
+  if (!aligned16(out)) return XQA_ERR_ALIGN;
+  uint8_t* base = reinterpret_cast<uint8_t*>(workspace);
+  xqa::CombineParams p;
+  p.out = reinterpret_cast<__half*>(out);
+  p.header = ws_i32(workspace);
+  p.seg_start = reinterpret_cast<const int32_t*>(base + r.ws.seg_start_off);
+  p.seg_bad = reinterpret_cast<const int32_t*>(base + r.ws.seg_bad_off);
+  p.partials = reinterpret_cast<const float*>(base + r.ws.partials_off);
+  p.num_q_heads = r.hq;
+  p.num_kv_heads = r.hkv;
+  p.group = r.group;
+  p.v_scale = v_scale;
+  cudaError_t e = xqa::launch_combine(p, r.nseg, (cudaStream_t)stream);
+  return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
+}
+
+xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens,
+                        float k_scale, float v_scale, void* out, const xqa_shape_t* shape,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return XQA_ERR_NULL;
+  Resolved r;
+  xqa_status_t st = resolve(shape, &r);
+  if (st != XQA_OK) return st;
+  if ((st = check_workspace(r, workspace, workspace_bytes)) != XQA_OK) return st;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return XQA_ERR_ALIGN;
+  if ((st = ensure_device_setup()) != XQA_OK) return st;
+  if ((st = xqa_plan(context_lens, shape, workspace, workspace_bytes, stream)) != XQA_OK)
+    return st;
+  if ((st = xqa_attend_partial(q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale,
+                               out, shape, workspace, workspace_bytes, stream)) != XQA_OK)
+    return st;
+  return xqa_combine(context_lens, v_scale, out, shape, workspace, workspace_bytes, stream);
+}
+
+xqa_status_t xqa_dequant_e5m2(const uint8_t* in, size_t n, float scale, uint16_t* out_fp16_bits,
+                              float* out_f32, void* stream) {
+  if (n == 0) return XQA_OK;
+  if (!in || !out_fp16_bits) return XQA_ERR_NULL;
+  cudaError_t e = xqa::launch_dequant(in, n, scale, out_fp16_bits, out_f32, (cudaStream_t)stream);
+  return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
+}
+
+xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void* stream) {
+  if (!workspace || !device_status) return XQA_ERR_NULL;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(device_status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return XQA_ERR_LAUNCH;
+  return XQA_OK;
+}
+
+xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int32_t* header,
+                           int32_t* seg_start, int32_t* seg_bad, void* stream) {
+  if (!workspace || !header || !seg_start) return XQA_ERR_NULL;
+  Resolved r;
+  xqa_status_t st = resolve(shape, &r);
+  if (st != XQA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const uint8_t* base = reinterpret_cast<const uint8_t*>(workspace);
+  if (cudaMemcpyAsync(header, base, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(seg_start, base + r.ws.seg_start_off, (size_t)(r.nseg + 1) * 4,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return XQA_ERR_LAUNCH;
+  if (seg_bad && cudaMemcpyAsync(seg_bad, base + r.ws.seg_bad_off, (size_t)r.nseg * 4,
+                                 cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return XQA_ERR_LAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return XQA_ERR_LAUNCH;
+  return XQA_OK;
+}
+
+const char* xqa_status_string(xqa_status_t status) {
+  switch (status) {
+    case XQA_OK: return "ok";
+    case XQA_ERR_NULL: return "a required pointer is NULL";
+    case XQA_ERR_SHAPE: return "unsupported or inconsistent dimensions";
+    case XQA_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case XQA_ERR_WORKSPACE: return "workspace smaller than xqa_workspace_size";
+    case XQA_ERR_LAUNCH: return "a CUDA call or kernel launch failed";
+    case XQA_ERR_DEVICE: return "no usable CUDA device";
+    case XQA_ERR_BAD_BLOCK_ID: return "device: block table entry outside [0, num_blocks)";
+    case XQA_ERR_CTX_TOO_LONG: return "device: context length < 0 or > max_blocks_per_seq*16";
+    case XQA_ERR_DEVICE_TIMEOUT: return "device: pipeline wait exceeded its time budget";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

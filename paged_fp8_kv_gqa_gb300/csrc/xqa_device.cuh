@@ -1,0 +1,199 @@
+// xqa_device.cuh — device-side building blocks shared by the libxqa kernels:
+// inline-PTX wrappers (mbarrier, TMA, warp MMA, movmatrix), the exact E5M2 ->
+// fp16 conversions, bounded pipeline waits and the workspace layout.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "xqa.h"
+
+namespace xqa {
+
+// ---------------------------------------------------------------------------
+// fixed geometry of the tuned path
+// ---------------------------------------------------------------------------
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 16;
+constexpr int kMaxGroup = 8;                                  // q heads per kv head (MMA N = 8)
+constexpr int kPageBytes = kBlockSize * kHeadDim;             // one (page, kv head) slice: 2048 B
+constexpr int kStageBytes = 2 * kPageBytes;                   // K slice + V slice
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;           // + 1 producer warp
+constexpr int kStages = 32;                                   // smem ring depth (multiple of 8)
+constexpr int kScratchStride = kHeadDim + 4;                  // floats per (warp, head) merge row
+constexpr int kScratchFloats = kConsumerWarps * kMaxGroup * kScratchStride;
+constexpr int kPartialSmem =
+    1024 /* alignment slack for the 1024-B swizzle atom */ + kStages * kStageBytes +
+    (kScratchFloats + 2 * kConsumerWarps * kMaxGroup) * 4;
+constexpr int kDefaultMinPagesPerCta = 8;
+constexpr int kPlanThreads = 1024;
+constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
+
+// Partial-result slot: O[8][128] unnormalised fp32, then M[8] (log2 domain), L[8].
+constexpr int kSlotFloats = kMaxGroup * kHeadDim + 2 * kMaxGroup;
+
+// A pipeline wait that has not completed after this long is treated as a fault.
+constexpr unsigned long long kWaitBudgetNs = 1000000000ull;  // 1 s
+
+// ---------------------------------------------------------------------------
+// workspace layout (int32 words, then 256-byte aligned fp32 partials)
+// ---------------------------------------------------------------------------
+struct WsLayout {
+  // header[0] status, [1] num_ctas, [2] total_pages, [3] num_segments
+  size_t seg_start_off;  // int32 [nseg + 1]
+  size_t seg_bad_off;    // int32 [nseg]
+  size_t partials_off;   // float [(n_max + nseg) * kSlotFloats]
+  size_t total;
+};
+
+__host__ __device__ inline WsLayout ws_layout(long long nseg, long long n_max) {
+  WsLayout l;
+  l.seg_start_off = 16;
+  l.seg_bad_off = l.seg_start_off + 4 * (size_t)(nseg + 1);
+  size_t end = l.seg_bad_off + 4 * (size_t)nseg;
+  l.partials_off = (end + 255) & ~(size_t)255;
+  l.total = l.partials_off + (size_t)(n_max + nseg) * kSlotFloats * sizeof(float);
+  return l;
+}
+
+// ---------------------------------------------------------------------------
+// small PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for phase `parity` of `bar`. Gives up (returns false) when *abort is
+// set by another warp or after kWaitBudgetNs; never spins without bound.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitBudgetNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// exact E5M2 -> fp16: the fp16 pattern of an E5M2 code is the code in the high
+// byte and zero in the low byte, so dequantisation is a byte permutation.
+// ---------------------------------------------------------------------------
+
+// Two codes of one 32-bit word that are adjacent along the contraction index:
+// bytes {0,1} (lo) or {2,3} (hi) of `w` -> half2 {w.b0<<8, w.b1<<8} etc.
+__device__ __forceinline__ uint32_t e5m2x2_lo(uint32_t w) { return prmt(w, 0u, 0x1404u); }
+__device__ __forceinline__ uint32_t e5m2x2_hi(uint32_t w) { return prmt(w, 0u, 0x3424u); }
+
+// Codes of two different words taken at the same byte position: interleave
+// {x.b0, x.b1, y.b0, y.b1} (or bytes 2,3), then widen each pair.
+__device__ __forceinline__ uint32_t interleave01(uint32_t x, uint32_t y) { return prmt(x, y, 0x5410u); }
+__device__ __forceinline__ uint32_t interleave23(uint32_t x, uint32_t y) { return prmt(x, y, 0x7632u); }
+// From an interleaved word {x_k, x_k+1, y_k, y_k+1}: half2 {x_k, y_k} / {x_k+1, y_k+1}.
+__device__ __forceinline__ uint32_t pair_even(uint32_t iw) { return prmt(iw, 0u, 0x2404u); }
+__device__ __forceinline__ uint32_t pair_odd(uint32_t iw) { return prmt(iw, 0u, 0x3414u); }
+
+__device__ __forceinline__ void record_status(int32_t* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+}  // namespace xqa

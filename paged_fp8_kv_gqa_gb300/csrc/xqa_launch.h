@@ -1,0 +1,43 @@
+// xqa_launch.h — host-side launch functions of the libxqa kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace xqa {
+
+struct PartialParams {
+  const __half* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  __half* out;
+  int32_t* header;           // workspace header (status, num_ctas, total_pages, nseg)
+  const int32_t* seg_start;  // [nseg + 1]
+  int32_t* seg_bad;          // [nseg]
+  float* partials;           // [(n_max + nseg) * kSlotFloats]
+  int batch, num_q_heads, num_kv_heads, group, max_blocks_per_seq, num_blocks;
+  float scale_log2;  // sm_scale * k_scale * log2(e)
+  float v_scale;
+};
+
+struct CombineParams {
+  __half* out;
+  const int32_t* header;
+  const int32_t* seg_start;
+  const int32_t* seg_bad;
+  const float* partials;
+  int num_q_heads, num_kv_heads, group;
+  float v_scale;
+};
+
+cudaError_t launch_plan(const int32_t* context_lens, int batch, int num_kv_heads,
+                        int max_blocks_per_seq, int n_max, int min_pages_per_cta,
+                        int32_t* workspace, cudaStream_t stream);
+cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                           const PartialParams& p, int n_max, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int num_segments, cudaStream_t stream);
+cudaError_t launch_dequant(const uint8_t* in, size_t n, float scale, uint16_t* out16,
+                           float* out32, cudaStream_t stream);
+
+}  // namespace xqa

@@ -1,0 +1,78 @@
+"""C ABI checks that need no GPU: the library builds, loads, exports every
+function include/xqa.h declares, and rejects bad host arguments before touching
+a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_fp8_kv_gqa_gb300 as xqa
+from paged_fp8_kv_gqa_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "xqa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return xqa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(xqa_[a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(xqa.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    nm = subprocess.run(["nm", "-D", "--defined-only", xqa.LIB_PATH], capture_output=True, text=True)
+    if nm.returncode == 0:
+        exported = set(re.findall(r"\bT\s+(xqa_\w+)", nm.stdout))
+        assert set(declared_functions()) <= exported
+
+
+def test_status_strings(lib):
+    for code in (0, 1, 2, 3, 4, 5, 6, 16, 17, 18):
+        s = xqa.xqa_status_string(code)
+        assert s and s != "unknown status"
+    assert xqa.xqa_status_string(12345) == "unknown status"
+
+
+def test_host_validation_without_device(lib):
+    shape = xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0)
+    n = ctypes.c_size_t(0)
+    assert lib.xqa_workspace_size(ctypes.byref(shape), ctypes.byref(n)) == xqa.XQA_OK
+    nseg = 64
+    head = 16 + 4 * (nseg + 1) + 4 * nseg
+    head = (head + 255) // 256 * 256
+    assert n.value == head + (152 + nseg) * (8 * 128 + 16) * 4
+    for bad in (
+        xqa.XqaShape(16, 32, 4, 64, 16, 1200, 22240, 0.0, 152, 0),   # head_dim
+        xqa.XqaShape(16, 32, 4, 128, 32, 1200, 22240, 0.0, 152, 0),  # block size
+        xqa.XqaShape(16, 30, 4, 128, 16, 1200, 22240, 0.0, 152, 0),  # Hq % Hkv
+        xqa.XqaShape(16, 64, 4, 128, 16, 1200, 22240, 0.0, 152, 0),  # G = 16
+        xqa.XqaShape(0, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0),   # batch
+        xqa.XqaShape(16, 32, 4, 128, 16, 1200, 2**28, 0.0, 152, 0),  # pool too large for int32 rows
+    ):
+        assert lib.xqa_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == xqa.XQA_ERR_SHAPE
+    assert lib.xqa_workspace_size(None, ctypes.byref(n)) == xqa.XQA_ERR_NULL
+    assert lib.xqa_decode(None, None, None, None, None, 1.0, 1.0, None, ctypes.byref(shape), None,
+                          0, None) == xqa.XQA_ERR_NULL
+    assert lib.xqa_dequant_e5m2(None, 0, 1.0, None, None, None) == xqa.XQA_OK
+    assert lib.xqa_dequant_e5m2(None, 5, 1.0, None, None, None) == xqa.XQA_ERR_NULL
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(xqa, "_lib", None)
+    monkeypatch.setattr(xqa, "LIB_PATH", "/nonexistent/libxqa.so")
+    with pytest.raises(RuntimeError, match="missing"):
+        xqa.load_library()

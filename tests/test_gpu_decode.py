@@ -1,0 +1,250 @@
+"""GPU parity tests of xqa_decode against the float64 oracle (through the C ABI).
+
+Tolerance: every fp16 output element must satisfy |gpu - ref| <= 2e-3 + 1e-2*|ref|
+(ref = unrounded float64 oracle). Plus bitwise properties: page relocation
+invariance and poisoned-memory invariance (the "bitwise randomized-page operator
+A/B" and boundary-context gates on the page "[Kernel][SM70] Pipeline batched E5M2
+XQA decode", section "Pending work and gates"), CUDA-graph replay with changed
+inputs (the changed-input graph replays on the page "[Kernel][WIP] Follow up
+FlashNext batch HC fusion and QSA route audit", section "Test Result"),
+determinism, and the device-side error paths.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_fp8_kv_gqa_gb300 as xqa
+from gpu_helpers import Dev, assert_close, oracle_of, oracle_out, run, to_dev, workload
+from oracle import e5m2, plan
+from paged_fp8_kv_gqa_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", wl.WORKLOADS)
+def test_workload_matches_oracle(name):
+    out = run(workload(name))
+    stats = assert_close(out, oracle_out(name), name)
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["b4_uniform_ctx1024", "b12_boundary"])
+def test_page_relocation_is_bitwise_invariant(name):
+    w = workload(name)
+    a = run(w)
+    b = run(wl.relocate_pages(w, seed=1234))
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_poisoned_memory_is_never_read():
+    w = workload("b12_boundary")
+    clean = run(w)
+    p = w.copy()
+    rng = np.random.default_rng(5)
+    used = set()
+    for b in range(p.batch):
+        n = (int(p.context_lens[b]) + 15) // 16
+        used.update(p.block_tables[b, :n].tolist())
+        # unused table entries: garbage, including out-of-range ids
+        tail = p.block_tables[b, n:]
+        tail[:] = rng.integers(-(2**31), 2**31 - 1, size=tail.shape, dtype=np.int64).astype(np.int32)
+    unused = np.setdiff1d(np.arange(p.num_blocks), sorted(used))
+    finite = wl.finite_e5m2_codes()
+    # unused pages and last-page tail slots: large finite codes instead of NaN
+    p.k_cache[unused] = 0x7B
+    p.v_cache[unused] = 0xFB
+    for b in range(p.batch):
+        ctx = int(p.context_lens[b])
+        if ctx % 16:
+            last = p.block_tables[b, (ctx + 15) // 16 - 1]
+            p.k_cache[last, :, ctx % 16:] = rng.choice(finite, size=p.k_cache[last, :, ctx % 16:].shape)
+            p.v_cache[last, :, ctx % 16:] = 0x7B
+    got = run(p)
+    assert np.array_equal(clean.view(np.uint16), got.view(np.uint16))
+
+
+def test_deterministic():
+    d = Dev(workload("b12_boundary"))
+    d.run()
+    a = d.result().copy()
+    d.run()
+    b = d.result()
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+@pytest.mark.parametrize("max_ctas,min_pages", [(1, 0), (2, 0), (7, 1), (37, 3), (0, 1), (300, 1)])
+def test_split_count_does_not_change_the_result(max_ctas, min_pages):
+    name = "b12_boundary"
+    out = run(workload(name), max_ctas=max_ctas, min_pages=min_pages)
+    assert_close(out, oracle_out(name), f"{name} max_ctas={max_ctas}")
+
+
+def test_single_token_context_is_the_v_row_bitwise():
+    w = wl.make_custom([1, 1, 1], 16, 2, seed=21, k_scale=0.5, v_scale=0.25)
+    out = run(w)
+    for b in range(3):
+        for h in range(16):
+            g = h // 8
+            page = w.block_tables[b, 0]
+            want = (e5m2.decode_fp16_view(w.v_cache[page, g, 0]) * w.v_scale).astype(np.float16)
+            assert np.array_equal(out[b, h].view(np.uint16), want.view(np.uint16))
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (16, 4), (8, 1), (24, 3), (2, 2)])
+def test_group_sizes(hq, hkv):
+    w = wl.make_custom([1, 16, 17, 300, 2049], hq, hkv, seed=hq * 100 + hkv)
+    assert_close(run(w), oracle_of(w), f"G={hq // hkv}")
+
+
+def test_zero_and_max_contexts():
+    w = wl.make_custom([0, 33, 0, 64], 8, 2, seed=3)
+    # the table row length equals the longest context exactly (ctx = MBS*16)
+    assert w.max_blocks_per_seq * 16 == 64
+    out = run(w)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0)
+    assert_close(out, oracle_of(w), "zero/max ctx")
+
+
+def test_all_contexts_zero():
+    w = wl.make_custom([0, 0], 8, 1, seed=4)
+    out = run(w)
+    assert np.all(out == 0)
+
+
+def test_custom_sm_scale():
+    w = wl.make_custom([100, 7], 8, 1, seed=8)
+    assert_close(run(w, sm_scale=0.02), oracle_of(w, sm_scale=0.02), "sm_scale")
+
+
+def test_plan_matches_oracle_bit_exactly():
+    for ctxs, hkv, mbs_extra, max_ctas, minp in [
+        ([256], 1, 0, 0, 0),
+        (list(wl.BOUNDARY_CONTEXTS), 4, 0, 0, 0),
+        ([5, 0, 17, 1000, 3], 2, 3, 5, 2),
+        (list(range(0, 3000, 97)), 3, 0, 152, 1),
+    ]:
+        w = wl.make_custom(ctxs, hkv * 2, hkv, seed=1)
+        d = Dev(w, max_ctas=max_ctas, min_pages=minp)
+        d.run()
+        got = xqa.xqa_read_plan(d.ws, d.shape)
+        n_max = max_ctas or torch.cuda.get_device_properties(0).multi_processor_count
+        ref = plan.plan(w.context_lens, hkv, w.max_blocks_per_seq, n_max, minp or 8)
+        assert got["status"] == 0
+        assert np.array_equal(got["seg_start"], ref["seg_start"])
+        assert np.array_equal(got["seg_bad"].astype(bool), ref["seg_bad"])
+        assert got["num_ctas"] == ref["num_ctas"]
+        assert got["total_pages"] == ref["total_pages"]
+        assert got["num_segments"] == ref["num_segments"]
+
+
+def test_cuda_graph_replay_with_changed_inputs():
+    w = workload("b12_boundary")
+    d = Dev(w)
+    d.run()
+    eager_first = d.result().copy()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        d.run(stream=s)  # warm-up on the capture stream
+        torch.cuda.current_stream().synchronize()
+        with torch.cuda.graph(g, stream=s):
+            d.run(stream=s)
+    torch.cuda.synchronize()
+    # 1) replay on unchanged inputs
+    d.out.fill_(float("nan"))
+    g.replay()
+    assert np.array_equal(d.result().view(np.uint16), eager_first.view(np.uint16))
+    # 2) change q, KV contents and context lengths in place (the plan changes)
+    # same shapes and scales (the scales are captured launch arguments)
+    w2 = wl.make_custom([5, 1, 4097, 32, 1025, 16385, 16, 17, 0, 3000, 1, 32768], 32, 4,
+                        seed=99, num_blocks=w.num_blocks, k_scale=w.k_scale, v_scale=w.v_scale,
+                        code_premul=4096.0)
+    assert w2.block_tables.shape == w.block_tables.shape
+    d.q.copy_(to_dev(w2.q))
+    d.k.copy_(to_dev(w2.k_cache))
+    d.v.copy_(to_dev(w2.v_cache))
+    d.bt.copy_(to_dev(w2.block_tables))
+    d.lens.copy_(to_dev(w2.context_lens))
+    d.out.fill_(float("nan"))
+    g.replay()
+    replayed = d.result().copy()
+    d.out.fill_(float("nan"))
+    d.run()
+    eager = d.result()
+    assert np.array_equal(replayed.view(np.uint16), eager.view(np.uint16))
+    assert_close(replayed, oracle_of(w2), "graph replay")
+
+
+# --------------------------------------------------------------------------
+# error paths
+# --------------------------------------------------------------------------
+
+def test_host_side_errors():
+    w = workload("tiny_b1_ctx256")
+    d = Dev(w)
+    with pytest.raises(xqa.XqaError) as e:
+        bad = xqa.XqaShape(1, 8, 1, 64, 16, 16, 16, 0.0, 0, 0)
+        xqa.xqa_workspace_size(bad)
+    assert e.value.code == xqa.XQA_ERR_SHAPE
+    with pytest.raises(xqa.XqaError) as e:
+        xqa.xqa_decode(d.q, d.k, d.v, d.bt, d.lens, 1.0, 1.0, out=d.out, workspace=d.ws[:64],
+                       shape=d.shape)
+    assert e.value.code == xqa.XQA_ERR_WORKSPACE
+    qbuf = torch.zeros(d.q.numel() + 8, dtype=torch.float16, device="cuda")
+    q_mis = qbuf[1:1 + d.q.numel()].view(d.q.shape)
+    with pytest.raises(xqa.XqaError) as e:
+        xqa.xqa_decode(q_mis, d.k, d.v, d.bt, d.lens, 1.0, 1.0, out=d.out, workspace=d.ws,
+                       shape=d.shape)
+    assert e.value.code == xqa.XQA_ERR_ALIGN
+    lib = xqa.load_library()
+    rc = lib.xqa_decode(None, d.k.data_ptr(), d.v.data_ptr(), d.bt.data_ptr(), d.lens.data_ptr(),
+                        1.0, 1.0, d.out.data_ptr(), d.shape, d.ws.data_ptr(), d.ws.numel(), None)
+    assert rc == xqa.XQA_ERR_NULL
+    gqa16 = xqa.XqaShape(1, 16, 1, 128, 16, 16, 16, 0.0, 0, 0)
+    with pytest.raises(xqa.XqaError) as e:
+        xqa.xqa_workspace_size(gqa16)
+    assert e.value.code == xqa.XQA_ERR_SHAPE
+
+
+def test_bad_block_id_is_reported_and_contained():
+    w = wl.make_custom([40, 300, 5000], 8, 2, seed=31)
+    ref = oracle_of(w)
+    w.block_tables[1, 3] = w.num_blocks + 7  # sequence 1 is bad, the others are not
+    d = Dev(w)
+    d.run()
+    out = d.result()
+    assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
+    assert np.all(np.isnan(out[1].astype(np.float32)))
+    assert_close(out[[0, 2]], ref[[0, 2]], "rows beside a bad block id")
+    # a later good call clears the status
+    d.bt.copy_(to_dev(wl.make_custom([40, 300, 5000], 8, 2, seed=31).block_tables))
+    d.run()
+    assert d.status() == xqa.XQA_OK
+
+
+def test_negative_block_id_is_reported():
+    w = wl.make_custom([40, 70], 8, 2, seed=32)
+    w.block_tables[0, 0] = -5
+    d = Dev(w, max_ctas=1)
+    d.run()
+    out = d.result()
+    assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
+    assert np.all(np.isnan(out[0].astype(np.float32)))
+    assert np.all(np.isfinite(out[1].astype(np.float32)))
+
+
+def test_context_longer_than_table_is_reported():
+    w = wl.make_custom([40, 70, 16], 8, 2, seed=33)
+    ref = oracle_of(w)
+    w.context_lens[1] = w.max_blocks_per_seq * 16 + 1
+    d = Dev(w)
+    d.run()
+    out = d.result()
+    assert d.status() == xqa.XQA_ERR_CTX_TOO_LONG
+    assert np.all(np.isnan(out[1].astype(np.float32)))
+    assert_close(out[[0, 2]], ref[[0, 2]], "rows beside a bad context length")
+    w.context_lens[1] = -3
+    d.lens.copy_(to_dev(w.context_lens))
+    d.run()
+    assert d.status() == xqa.XQA_ERR_CTX_TOO_LONG
