@@ -37,7 +37,8 @@ def decode_closed_form(codes) -> np.ndarray:
 def decode_fp16_view(codes) -> np.ndarray:
     """Value of each code via the fp16 bit pattern ``code << 8``, widened to float64."""
     x = np.asarray(codes, dtype=np.uint8).astype(np.uint16) << np.uint16(8)
-    return x.view(np.float16).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        return x.view(np.float16).astype(np.float64)
 
 
 def fp16_bits(codes) -> np.ndarray:
