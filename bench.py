@@ -308,12 +308,13 @@ def run_gpu(args, world, rank, local, dist):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(dist)
-    t0.record(stream)
-    for _ in range(nrep):
-        g_main.replay()
-    if g_tail is not None:
-        g_tail.replay()
-    t1.record(stream)
+    with torch.cuda.stream(stream):  # graph replays launch on the current stream
+        t0.record(stream)
+        for _ in range(nrep):
+            g_main.replay()
+        if g_tail is not None:
+            g_tail.replay()
+        t1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
     barrier(dist)
@@ -334,9 +335,10 @@ def run_gpu(args, world, rank, local, dist):
                     xqa.xqa_attend_partial(q, k, v, bt, lens, w.k_scale, w.v_scale, out, ws,
                                            shape, stream)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        gp.replay()
-        b.record(stream)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            gp.replay()
+            b.record(stream)
         stream.synchronize()
         part_ms = [a.elapsed_time(b) / C]
         timing_note = "partial-only graph replay (no event nodes in this torch)"

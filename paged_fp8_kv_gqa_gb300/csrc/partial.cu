@@ -6,26 +6,30 @@
 // E5M2 conversion, shared-memory publication, QK, V load + conversion, PV and
 // synchronization. That page's starting kernel was memory-latency bound
 // (long-scoreboard stalls at low occupancy, section "Starting bottleneck"); on
-// sm_103a this kernel keeps up to kStages pages in flight per SM instead:
+// sm_103a this kernel keeps kStages pages in flight per SM instead.
 //
-//  * producer warp: walks the block table (bounds-checked) and issues, per
-//    page, two 2-D TMA loads (K slice and V slice, 2048 B each, 128-byte
-//    swizzle) into a kStages-deep shared-memory ring; mbarrier full/empty
-//    pairs publish the stages;
-//  * 8 consumer warps: warp w takes ring stages w, w+8, ...; per 16-token page
-//      - reads K and V with conflict-free 16-byte shared loads,
-//      - dequantises exactly (fp16 pattern = code << 8, a byte permutation),
-//      - S^T[16 tok x 8 heads] = K * Q^T with 8 m16n8k16 MMAs (fp32 accumulate),
-//      - online softmax in the log2 domain (k_scale and sm_scale folded into
-//        one fp32 logit scale; the running max only moves when a logit exceeds
-//        it by more than 8, so most pages skip the rescale),
-//      - P^T to the B-operand layout with two movmatrix transposes,
-//      - O^T[128 x 8] += V^T * P^T with 8 MMAs plus one MMA against ones for the
-//        row sums l (so l sums exactly the fp16 P used for O);
-//  * at the end of every segment the 8 warps' (m, l, O) are merged in shared
-//    memory; a segment owned whole by this CTA is normalised and written as fp16
-//    (out = O * (v_scale / l)); otherwise the piece goes to partial slot i + s
-//    for the combine kernel.
+// Every one of the 8 warps both loads and computes. Warp w owns the CTA-local
+// pages w, w+8, w+16, ... and the ring slots w, w+8, w+16, w+24 they map to
+// (slot = page % kStages). It keeps kLookahead of its pages in flight: after
+// computing page q it issues the two 2-D TMA loads (K and V slice, 2048 B each,
+// 128-byte swizzle) of its page q + kStages into the slot it just freed, so no
+// empty-slot barrier is needed and TMA issue is spread over all warps. Block ids
+// are fetched 32 owned pages at a time, one batch ahead (bounds-checked).
+//
+// Per 16-token page a warp
+//   - reads K and V with conflict-free 16-byte shared loads,
+//   - dequantises exactly (fp16 pattern = code << 8, a byte permutation),
+//   - S^T[16 tok x 8 heads] = K * Q^T with 8 m16n8k16 MMAs (fp32 accumulate),
+//   - runs the online softmax in the log2 domain (k_scale and sm_scale folded
+//     into one fp32 logit scale; the running max only moves when a logit
+//     exceeds it by more than 8, so most pages skip the rescale),
+//   - moves P^T to the B-operand layout with two movmatrix transposes,
+//   - O^T[128 x 8] += V^T * P^T with 8 MMAs plus one MMA against ones for the
+//     row sums l (so l sums exactly the fp16 P used for O).
+// At the end of every segment the 8 warps' (m, l, O) are merged in shared
+// memory; a segment owned whole by this CTA is normalised and written as fp16
+// (out = O * (v_scale / l)); otherwise the piece goes to partial slot i + s for
+// the combine kernel.
 //
 // Contraction-index permutation: the MMA result does not depend on how the
 // contraction index is laid out, as long as both operands use the same layout.
@@ -47,7 +51,7 @@ constexpr uint32_t kOnesHalf2 = 0x3C003C00u;
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
 
 __device__ __forceinline__ int consumer_bar_or(int pred) {
@@ -58,20 +62,67 @@ __device__ __forceinline__ int consumer_bar_or(int pred) {
       "bar.red.or.pred q, 1, %2, p;\n\t"
       "selp.s32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred), "n"(kConsumerWarps * 32)
+      : "r"(pred), "n"(kThreads)
       : "memory");
   return r;
 }
 
-// Largest s in [0, nseg) with seg_start[s] <= page (seg_start[nseg] > page).
-__device__ __forceinline__ int find_segment(const int32_t* seg_start, int nseg, int page) {
-  int lo = 0, hi = nseg - 1;
+// Largest s in [lo, nseg) with seg_start[s] <= page, given seg_start[lo] <= page
+// < seg_start[nseg]. `seg_start` may point to shared or global memory.
+__device__ __forceinline__ int find_segment(const int32_t* seg_start, int lo, int nseg, int page) {
+  int hi = nseg - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(&seg_start[mid]) <= page) lo = mid;
+    if (seg_start[mid] <= page) lo = mid;
     else hi = mid - 1;
   }
   return lo;
+}
+
+// TMA coordinates of 32 consecutive owned pages of one warp, one per lane.
+struct PageBatch {
+  int y;    // row of the (page, kv head) slice in the [NB*Hkv*16, 128] view
+  int bad;  // block id outside [0, NB)
+  int seg;  // segment of the page
+};
+
+__device__ __forceinline__ PageBatch load_batch(const PartialParams& p, const int32_t* segs,
+                                                int s_first, int nseg, int cbeg, int npages,
+                                                int warp, int base, int lane) {
+  PageBatch r{0, 0, s_first};
+  const int q = warp + kWarps * (base + lane);
+  if (q < npages) {
+    const int pg = cbeg + q;
+    const int s = find_segment(segs, s_first, nseg, pg);
+    const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+    const int j = pg - segs[s];
+    const int id = __ldg(&p.block_tables[(size_t)b * p.max_blocks_per_seq + j]);
+    r.bad = (id < 0 || id >= p.num_blocks) ? 1 : 0;
+    r.y = r.bad ? 0 : (id * p.num_kv_heads + kvh) * kBlockSize;
+    r.seg = s;
+  }
+  return r;
+}
+
+// Q of segment s as B fragments: lane (g, c) holds head g, dims [32c, 32c+32).
+__device__ __forceinline__ void load_q(const PartialParams& p, int s, int g, int c,
+                                       uint32_t (&qf)[16]) {
+  const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+  if (g < p.group) {
+    const uint4* qp = reinterpret_cast<const uint4*>(
+        p.q + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + g) * kHeadDim + 32 * c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(qp + i);
+      qf[4 * i] = v.x;
+      qf[4 * i + 1] = v.y;
+      qf[4 * i + 2] = v.z;
+      qf[4 * i + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qf[i] = 0u;
+  }
 }
 
 struct WarpState {
@@ -94,7 +145,7 @@ __device__ __forceinline__ void reset_state(WarpState& st) {
 // One 16-token page of one kv head: QK, online softmax, PV.
 __device__ __forceinline__ void process_page(WarpState& st, const uint8_t* ks, const uint8_t* vs,
                                              const uint32_t (&qf)[16], int nvalid, float scale_log2,
-                                             int g, int c, uint64_t* empty_bar, int lane) {
+                                             int g, int c) {
   // ---- K and V shared loads (swizzled 16-byte chunks) ----
   const int kc0 = ((2 * c) ^ g) << 4, kc1 = ((2 * c + 1) ^ g) << 4;
   const uint4 ka0 = lds128(ks + g * 128 + kc0);
@@ -173,9 +224,6 @@ __device__ __forceinline__ void process_page(WarpState& st, const uint8_t* ks, c
     mma_16816(st.o[2 * u + 1], pair_even(xy23), pair_odd(xy23), pair_even(zw23), pair_odd(zw23),
               pb0, pb1);
   }
-  // every shared byte of this stage is in registers and consumed: release it
-  __syncwarp();
-  if (lane == 0) mbar_arrive(empty_bar);
   mma_16816(st.l, kOnesHalf2, kOnesHalf2, kOnesHalf2, kOnesHalf2, pb0, pb1);
 }
 
@@ -186,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const PartialParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
-  __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ int stage_bad[kStages];
   __shared__ int abort_flag;
 
@@ -203,127 +250,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* scratch = reinterpret_cast<float*>(stages + kStages * kStageBytes);
   float* scr_m = scratch + kScratchFloats;
-  float* scr_l = scr_m + kConsumerWarps * kMaxGroup;
+  float* scr_l = scr_m + kWarps * kMaxGroup;
+  int32_t* seg_cache = reinterpret_cast<int32_t*>(scr_l + kWarps * kMaxGroup);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
-    }
+    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
     abort_flag = 0;
     fence_mbar_init();
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
   }
+  const bool segs_in_smem = nseg + 1 <= kSegCache;
+  if (segs_in_smem)
+    for (int i = tid; i <= nseg; i += kThreads) seg_cache[i] = __ldg(&p.seg_start[i]);
   __syncthreads();
-
-  const int s_first = find_segment(p.seg_start, nseg, cbeg);
+  const int32_t* segs = segs_in_smem ? seg_cache : p.seg_start;
+  const int s_first = find_segment(segs, 0, nseg, cbeg);
   volatile int* abort = &abort_flag;
-
-  if (warp == kConsumerWarps) {
-    // ======================= producer warp =======================
-    const uint64_t policy = l2_evict_first_policy();
-    int s_cur = s_first;
-    bool aborted = false;
-    int issued = 0;
-    for (int base = 0; base < npages && !aborted; base += 32) {
-      const int qi = base + lane;
-      const int pg = cbeg + qi;
-      int s = s_cur, y = 0, bad = 0;
-      if (qi < npages) {
-        while (__ldg(&p.seg_start[s + 1]) <= pg) ++s;
-        const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
-        const int j = pg - __ldg(&p.seg_start[s]);
-        const int id = __ldg(&p.block_tables[(size_t)b * p.max_blocks_per_seq + j]);
-        bad = (id < 0 || id >= p.num_blocks) ? 1 : 0;
-        y = bad ? 0 : (id * p.num_kv_heads + kvh) * kBlockSize;
-      }
-      const int cnt = min(32, npages - base);
-      for (int l = 0; l < cnt; ++l) {
-        const int qq = base + l;
-        const int slot = qq % kStages, use = qq / kStages;
-        const int yl = __shfl_sync(kFull, y, l);
-        const int badl = __shfl_sync(kFull, bad, l);
-        const int sl = __shfl_sync(kFull, s, l);
-        if (use > 0) {
-          const bool ok = mbar_wait_bounded(&empty_bar[slot], (use - 1) & 1, abort);
-          if (!__all_sync(kFull, ok)) {  // warp-uniform outcome
-            aborted = true;
-            break;
-          }
-        }
-        if (lane == 0) {
-          uint8_t* st = stages + slot * kStageBytes;
-          stage_bad[slot] = badl;
-          if (badl) {
-            atomicOr(&p.seg_bad[sl], 1);
-            record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
-            mbar_arrive(&full_bar[slot]);
-          } else {
-            mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
-            tma_load_2d(st, &tm_k, &full_bar[slot], 0, yl, policy);
-            tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, yl, policy);
-          }
-        }
-        __syncwarp();
-        issued = qq + 1;
-      }
-      s_cur = __shfl_sync(kFull, s, cnt - 1);
-    }
-    if (aborted && lane == 0) {
-      *abort = 1;
-      record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
-    }
-    // Drain: every copy this warp issued must land before the warp exits, so no
-    // bulk copy can outlive the CTA's shared memory even if consumers gave up.
-    // The last kStages issued stages are the only ones that can be in flight.
-    {
-      int never = 0;
-      volatile int* no_abort = &never;
-      for (int qq = issued > kStages ? issued - kStages : 0; qq < issued; ++qq) {
-        const bool ok = mbar_wait_bounded(&full_bar[qq % kStages], (qq / kStages) & 1, no_abort);
-        if (!__all_sync(kFull, ok)) {
-          if (lane == 0) record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
-          break;
-        }
-      }
-    }
-    return;
-  }
-
-  // ======================= consumer warps =======================
+  const uint64_t policy = l2_evict_first_policy();
   const int g = lane >> 2, c = lane & 3;
+
+  // ---- this warp's loads: owned page k is CTA-local page warp + 8k ----
+  const int owned = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
+  PageBatch cur = load_batch(p, segs, s_first, nseg, cbeg, npages, warp, 0, lane);
+  PageBatch nxt = load_batch(p, segs, s_first, nseg, cbeg, npages, warp, 32, lane);
+  int cur_base = 0;
+  int issued = 0;  // owned pages whose loads have been issued
+  auto issue_next = [&]() {
+    if (issued >= owned) return;
+    const int k = issued++;
+    if (k >= cur_base + 32) {
+      cur = nxt;
+      cur_base += 32;
+      nxt = load_batch(p, segs, s_first, nseg, cbeg, npages, warp, cur_base + 32, lane);
+    }
+    const int y = __shfl_sync(kFull, cur.y, k - cur_base);
+    const int bad = __shfl_sync(kFull, cur.bad, k - cur_base);
+    const int sg = __shfl_sync(kFull, cur.seg, k - cur_base);
+    const int slot = (warp + kWarps * k) % kStages;
+    __syncwarp();  // all lanes' reads of this slot's previous page are done
+    if (lane == 0) {
+      uint8_t* st = stages + slot * kStageBytes;
+      stage_bad[slot] = bad;
+      fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
+      if (bad) {
+        atomicOr(&p.seg_bad[sg], 1);
+        record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
+        mbar_arrive(&full_bar[slot]);
+      } else {
+        mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
+        tma_load_2d(st, &tm_k, &full_bar[slot], 0, y, policy);
+        tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, y, policy);
+      }
+    }
+    __syncwarp();
+  };
+#pragma unroll 1
+  for (int i = 0; i < kLookahead; ++i) issue_next();
+
   WarpState st;
+  uint32_t qf[16], qf_next[16];
+  int q_next_seg = -1;
   int s = s_first;
   int q0 = 0;
   while (q0 < npages) {
-    while (__ldg(&p.seg_start[s + 1]) <= cbeg + q0) ++s;
-    const int sb = __ldg(&p.seg_start[s]), se = __ldg(&p.seg_start[s + 1]);
+    while (segs[s + 1] <= cbeg + q0) ++s;
+    const int sb = segs[s], se = segs[s + 1];
     const int qe = min(se, cend) - cbeg;
     const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
     const int ctx = __ldg(&p.context_lens[b]);
     const bool whole = (sb >= cbeg) && (se <= cend);
-
-    uint32_t qf[16];
-    if (g < p.group) {
-      const uint4* qp = reinterpret_cast<const uint4*>(
-          p.q + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + g) * kHeadDim + 32 * c);
+    if (q_next_seg == s) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = __ldg(qp + i);
-        qf[4 * i] = v.x;
-        qf[4 * i + 1] = v.y;
-        qf[4 * i + 2] = v.z;
-        qf[4 * i + 3] = v.w;
-      }
+      for (int i = 0; i < 16; ++i) qf[i] = qf_next[i];
     } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) qf[i] = 0u;
+      load_q(p, s, g, c, qf);
+    }
+    if (qe < npages) {  // prefetch Q of the next segment this CTA works on
+      q_next_seg = find_segment(segs, s, nseg, cbeg + qe);
+      load_q(p, q_next_seg, g, c, qf_next);
     }
     reset_state(st);
     int poisoned = 0;
 
-    for (int q = q0 + ((warp - q0 % kConsumerWarps) + kConsumerWarps) % kConsumerWarps; q < qe;
-         q += kConsumerWarps) {
+    for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe; q += kWarps) {
       const int slot = q % kStages;
       const bool ready = mbar_wait_bounded(&full_bar[slot], (q / kStages) & 1, abort);
       if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
@@ -336,15 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (stage_bad[slot]) {
         poisoned = 1;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
-        continue;
+      } else {
+        const int j = cbeg + q - sb;
+        const int nvalid = min(kBlockSize, ctx - j * kBlockSize);
+        const uint8_t* stg = stages + slot * kStageBytes;
+        process_page(st, stg, stg + kPageBytes, qf, nvalid, p.scale_log2, g, c);
       }
-      const int j = cbeg + q - sb;
-      const int nvalid = min(kBlockSize, ctx - j * kBlockSize);
-      const uint8_t* stg = stages + slot * kStageBytes;
-      process_page(st, stg, stg + kPageBytes, qf, nvalid, p.scale_log2, g, c, &empty_bar[slot],
-                   lane);
+      // refill the slot just freed with page q + kStages (warp-uniform decision)
+      if (!__any_sync(kFull, *abort != 0)) issue_next();
     }
 
     // ---- merge the 8 warps' states for this segment ----
@@ -371,11 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int dq = (tid & 31) * 4;   // 0..124
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, scr_m[w * kMaxGroup + h]);
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, scr_m[w * kMaxGroup + h]);
       float L = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < kWarps; ++w) {
         const float mw = scr_m[w * kMaxGroup + h];
         const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
         L += sc * scr_l[w * kMaxGroup + h];
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (whole) {
           __half* o = p.out +
                       ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim + dq;
-          float r = p.v_scale / L;
+          const float r = p.v_scale / L;
           uint2 v;
           if (any_poison) {
             const float nan = __int_as_float(0x7fc00000);
@@ -415,6 +425,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     consumer_bar();  // scratch is reused by the next segment
     q0 = qe;
     ++s;
+  }
+
+  // Drain: after an abort some issued copies may not have been waited for; every
+  // copy must land before the CTA's shared memory is released.
+  if (*abort) {
+    int never = 0;
+    volatile int* no_abort = &never;
+    // only the last kLookahead issued pages can still be in flight: every
+    // earlier one was waited for before its slot was reissued
+    const int first = issued > kLookahead ? issued - kLookahead : 0;
+    for (int k = first; k < issued; ++k) {
+      const int q = warp + kWarps * k;
+      const bool ok = mbar_wait_bounded(&full_bar[q % kStages], (q / kStages) & 1, no_abort);
+      if (!__all_sync(kFull, ok)) break;
+    }
   }
 }
 

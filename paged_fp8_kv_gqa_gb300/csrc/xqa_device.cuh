@@ -19,14 +19,16 @@ constexpr int kBlockSize = 16;
 constexpr int kMaxGroup = 8;                                  // q heads per kv head (MMA N = 8)
 constexpr int kPageBytes = kBlockSize * kHeadDim;             // one (page, kv head) slice: 2048 B
 constexpr int kStageBytes = 2 * kPageBytes;                   // K slice + V slice
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;           // + 1 producer warp
-constexpr int kStages = 32;                                   // smem ring depth (multiple of 8)
+constexpr int kWarps = 8;                                     // every warp loads and computes
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 32;                                   // smem ring depth (multiple of kWarps)
+constexpr int kLookahead = kStages / kWarps;                  // pages in flight per warp
 constexpr int kScratchStride = kHeadDim + 4;                  // floats per (warp, head) merge row
-constexpr int kScratchFloats = kConsumerWarps * kMaxGroup * kScratchStride;
+constexpr int kScratchFloats = kWarps * kMaxGroup * kScratchStride;
+constexpr int kSegCache = 2048;                               // seg_start entries kept in smem
 constexpr int kPartialSmem =
     1024 /* alignment slack for the 1024-B swizzle atom */ + kStages * kStageBytes +
-    (kScratchFloats + 2 * kConsumerWarps * kMaxGroup) * 4;
+    (kScratchFloats + 2 * kWarps * kMaxGroup) * 4 + kSegCache * 4;
 constexpr int kDefaultMinPagesPerCta = 8;
 constexpr int kPlanThreads = 1024;
 constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
@@ -115,6 +117,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitBudgetNs) return false;
   }
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
