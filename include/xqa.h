@@ -133,6 +133,40 @@ xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void
 xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int32_t* header,
                            int32_t* seg_start, int32_t* seg_bad, void* stream);
 
+/* Size of the device array behind xqa_decode_static_workspace (per device). */
+#define XQA_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
+
+/* xqa_decode for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point. It exists for callers that
+ * are not allowed to call cudaMalloc: a plugin inside a host runtime that owns
+ * all device memory through its own pool, a latency-critical path where an
+ * allocation (which may synchronise the device) is forbidden, or an operator
+ * interface that passes only inputs and outputs and has no workspace hook.
+ *
+ * Arguments and results are those of xqa_decode, minus the workspace: the
+ * split-KV scratch comes from a fixed XQA_STATIC_WORKSPACE_BYTES array in the
+ * library's device image, which every device that loads the library holds
+ * until the process exits. Nothing is allocated and nothing needs clearing
+ * (each call's planner rewrites every scratch word the call reads).
+ *
+ *   - Shapes whose xqa_workspace_size exceeds XQA_STATIC_WORKSPACE_BYTES are
+ *     rejected with XQA_ERR_WORKSPACE before anything is enqueued (for 152
+ *     SMs: B * Hkv up to about 1800 segments).
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (that device must be current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array: calls that may overlap on the
+ *     GPU (different streams without ordering, or threads racing on one device)
+ *     race on it and corrupt each other. Order them, e.g. on one stream.
+ *   - The device status word lives in the shared array and is not exposed;
+ *     rows affected by a bad block id or context length still come back NaN. */
+xqa_status_t xqa_decode_static_workspace(const void* q, const uint8_t* k_cache,
+                                         const uint8_t* v_cache, const int32_t* block_tables,
+                                         const int32_t* context_lens, float k_scale,
+                                         float v_scale, void* out, const xqa_shape_t* shape,
+                                         void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* xqa_status_string(xqa_status_t status);
 

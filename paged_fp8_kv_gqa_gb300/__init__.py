@@ -41,6 +41,7 @@ EXPORTED = (
     "xqa_read_status",
     "xqa_read_plan",
     "xqa_status_string",
+    "xqa_decode_static_workspace",
 )
 
 
@@ -83,6 +84,7 @@ _SIGS = {
     "xqa_read_status": [_P, ctypes.POINTER(ctypes.c_int32), _P],
     "xqa_read_plan": [_P, _SHAPE, _P, _P, _P, _P],
     "xqa_status_string": [ctypes.c_int],
+    "xqa_decode_static_workspace": [_P, _P, _P, _P, _P, _F, _F, _P, _SHAPE, _P],
 }
 
 
@@ -238,3 +240,28 @@ def xqa_read_plan(workspace: torch.Tensor, shape: XqaShape, stream=None) -> dict
                                         _stream_handle(stream)), "xqa_read_plan")
     return {"status": int(header[0]), "num_ctas": int(header[1]), "total_pages": int(header[2]),
             "num_segments": int(header[3]), "seg_start": seg_start, "seg_bad": seg_bad}
+
+
+def xqa_decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens, k_scale: float,
+                                v_scale: float, out=None, shape: XqaShape | None = None,
+                                stream=None, sm_scale: float = 0.0, max_ctas: int = 0,
+                                min_pages_per_cta: int = 0):
+    """xqa_decode without a workspace argument, for callers that may not allocate
+    device memory: the scratch is the library's fixed per-device array (see
+    include/xqa.h). Calls that may overlap on one device must be ordered."""
+    if shape is None:
+        shape = make_shape(q, k_cache, block_tables, sm_scale, max_ctas, min_pages_per_cta)
+    if out is None:
+        out = torch.empty_like(q)
+    ptrs = (
+        _cuda(q, torch.float16, "q"),
+        _cuda(k_cache, torch.uint8, "k_cache"),
+        _cuda(v_cache, torch.uint8, "v_cache"),
+        _cuda(block_tables, torch.int32, "block_tables"),
+        _cuda(context_lens, torch.int32, "context_lens"),
+        _cuda(out, torch.float16, "out"),
+    )
+    _check(load_library().xqa_decode_static_workspace(
+        ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], float(k_scale), float(v_scale), ptrs[5],
+        ctypes.byref(shape), _stream_handle(stream)), "xqa_decode_static_workspace")
+    return out
