@@ -66,6 +66,10 @@ typedef struct xqa_shape {
   float sm_scale;             /* softmax scale; <= 0 selects 1/sqrt(D) */
   int32_t max_ctas;           /* upper bound on split-KV CTAs; 0 = SM count */
   int32_t min_pages_per_cta;  /* planner lower bound on pages per CTA; 0 = 8 */
+  int32_t merge_mode;         /* how segments split over several CTAs are merged:
+                                 0 = by the last CTA to finish one (inside the
+                                 partial kernel, default); 1 = by the separate
+                                 combine kernel (xqa_combine) */
 } xqa_shape_t;
 
 /* Bytes of device workspace xqa_decode needs for `shape` on the current
@@ -91,7 +95,8 @@ xqa_status_t xqa_workspace_size(const xqa_shape_t* shape, size_t* bytes);
  *
  * out[b, h, :] = sum_t softmax_t(sm_scale * <q[b,h], k_t>) * v_t over the
  * ctx_b tokens of kv head h / G, rounded to fp16 (round to nearest even).
- * Three kernels are enqueued: planner, split-KV partial, log-sum-exp combine.
+ * Kernels enqueued: planner, split-KV partial (which also merges split
+ * segments when merge_mode is 0), and with merge_mode 1 the log-sum-exp combine.
  * No host synchronisation; the call may be captured into a CUDA graph.
  * Concurrent calls must not share a workspace. */
 xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
@@ -101,7 +106,10 @@ xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_
 
 /* The three stages of xqa_decode, exposed separately so they can be timed one
  * by one. Called in this order with the same arguments they are exactly
- * xqa_decode. */
+ * xqa_decode. xqa_attend_partial is launched as a programmatic dependent of
+ * the previous kernel on the stream (normally xqa_plan's) and must follow
+ * xqa_plan on the same workspace. With merge_mode 0 the partial kernel merges
+ * split segments itself and xqa_combine enqueues nothing. */
 xqa_status_t xqa_plan(const int32_t* context_lens, const xqa_shape_t* shape, void* workspace,
                       size_t workspace_bytes, void* stream);
 xqa_status_t xqa_attend_partial(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,

@@ -59,6 +59,7 @@ class XqaShape(ctypes.Structure):
         ("sm_scale", ctypes.c_float),
         ("max_ctas", ctypes.c_int32),
         ("min_pages_per_cta", ctypes.c_int32),
+        ("merge_mode", ctypes.c_int32),
     ]
 
 
@@ -132,14 +133,16 @@ def _cuda(t: torch.Tensor, dtype, name: str) -> int:
 
 
 def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
-               sm_scale: float = 0.0, max_ctas: int = 0, min_pages_per_cta: int = 0) -> XqaShape:
+               sm_scale: float = 0.0, max_ctas: int = 0, min_pages_per_cta: int = 0,
+               merge_mode: int = 0) -> XqaShape:
     """Shape descriptor from q [B, Hq, D], k_cache [NB, Hkv, BS, D], block_tables [B, MBS]."""
     b, hq, d = q.shape
     nb, hkv, bs, d2 = k_cache.shape
     if d2 != d or block_tables.shape[0] != b:
         raise ValueError("inconsistent q / k_cache / block_tables shapes")
     return XqaShape(int(b), int(hq), int(hkv), int(d), int(bs), int(block_tables.shape[1]),
-                    int(nb), float(sm_scale), int(max_ctas), int(min_pages_per_cta))
+                    int(nb), float(sm_scale), int(max_ctas), int(min_pages_per_cta),
+                    int(merge_mode))
 
 
 def xqa_workspace_size(shape: XqaShape) -> int:

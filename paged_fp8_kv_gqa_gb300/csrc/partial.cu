@@ -227,6 +227,44 @@ __device__ __forceinline__ void process_page(WarpState& st, const uint8_t* ks, c
   mma_16816(st.l, kOnesHalf2, kOnesHalf2, kOnesHalf2, kOnesHalf2, pb0, pb1);
 }
 
+// LSE merge of all pieces of split segment s into fp16 rows (thread: head h,
+// dims dq..dq+3). Pieces were written by other CTAs: read through L2.
+__device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int sb, int se,
+                                             int total, int n, int h, int dq) {
+  if (h >= p.group) return;
+  const int ilo = cta_of_page(sb, total, n), ihi = cta_of_page(se - 1, total, n);
+  const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+  __half* o = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim + dq;
+  uint2 v;
+  if (__ldcg(&p.seg_bad[s]) != 0) {
+    const float nan = __int_as_float(0x7fc00000);
+    v.x = pack_half2(nan, nan);
+    v.y = v.x;
+    *reinterpret_cast<uint2*>(o) = v;
+    return;
+  }
+  float M = -INFINITY;
+  for (int i = ilo; i <= ihi; ++i)
+    M = fmaxf(M, __ldcg(p.partials + (size_t)(i + s) * kSlotFloats + kMaxGroup * kHeadDim + h));
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = ilo; i <= ihi; ++i) {
+    const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
+    const float mi = __ldcg(slot + kMaxGroup * kHeadDim + h);
+    const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
+    L += w * __ldcg(slot + kMaxGroup * kHeadDim + kMaxGroup + h);
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(slot + h * kHeadDim + dq));
+    acc.x += w * x.x;
+    acc.y += w * x.y;
+    acc.z += w * x.z;
+    acc.w += w * x.w;
+  }
+  const float r = p.v_scale / L;
+  v.x = pack_half2(acc.x * r, acc.y * r);
+  v.y = pack_half2(acc.z * r, acc.w * r);
+  *reinterpret_cast<uint2*>(o) = v;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -237,13 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int stage_bad[kStages];
   __shared__ int abort_flag;
 
-  const int n = p.header[1];
+  __shared__ int scan_warp[kWarps];
+  __shared__ int scan_carry;
+  __shared__ int merge_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
-  if (cta >= n) return;
-  const long long total = p.header[2];
-  const int cbeg = (int)(((long long)cta * total) / n);
-  const int cend = (int)(((long long)(cta + 1) * total) / n);
-  const int npages = cend - cbeg;
   const int nseg = p.batch * p.num_kv_heads;
 
   uint8_t* stages = reinterpret_cast<uint8_t*>(
@@ -253,7 +290,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* scr_l = scr_m + kWarps * kMaxGroup;
   int32_t* seg_cache = reinterpret_cast<int32_t*>(scr_l + kWarps * kMaxGroup);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // ---- the plan: computed here when the segment table fits in shared memory
+  // (same integer rule as the planner kernel), else read from the planner ----
+  const bool segs_in_smem = nseg + 1 <= kSegCache;
+  const int32_t* segs;
+  int total, n;
+  if (segs_in_smem) {
+    if (tid == 0) scan_carry = 0;
+    __syncthreads();
+    const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
+    for (int base = 0; base < p.batch; base += kThreads) {
+      const int b = base + tid;
+      int pages = 0;
+      if (b < p.batch) {
+        const int ctx = __ldg(&p.context_lens[b]);
+        pages = (ctx < 0 || (long long)ctx > max_ctx) ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
+      }
+      int incl = pages;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += u;
+      }
+      if (lane == 31) scan_warp[warp] = incl;
+      __syncthreads();
+      int before = scan_carry;
+      for (int w = 0; w < warp; ++w) before += scan_warp[w];
+      const int excl = before + incl - pages;
+      if (b < p.batch)
+        for (int h = 0; h < p.num_kv_heads; ++h)
+          seg_cache[b * p.num_kv_heads + h] = excl * p.num_kv_heads + h * pages;
+      __syncthreads();
+      if (tid == kThreads - 1) scan_carry = excl + pages;
+      __syncthreads();
+    }
+    total = scan_carry * p.num_kv_heads;
+    if (tid == 0) seg_cache[nseg] = total;
+    n = num_ctas_for(total, p.n_max, p.min_pages);
+    segs = seg_cache;
+  } else {
+    griddep_wait();
+    total = p.header[2];
+    n = p.header[1];
+    segs = p.seg_start;
+  }
+  __syncthreads();
+
+  // ---- rows of empty segments (context length 0, or invalid -> NaN) ----
+  if (cta == 0) {
+    const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
+    for (int s = warp; s < nseg; s += kWarps) {
+      if (segs[s] != segs[s + 1]) continue;
+      const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+      const int ctx = __ldg(&p.context_lens[b]);
+      const bool bad = ctx < 0 || (long long)ctx > max_ctx;
+      const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
+      uint4 val;
+      val.x = val.y = val.z = val.w = pack_half2(v, v);
+      for (int i = lane; i < p.group * (kHeadDim / 8); i += 32) {
+        const int h = i / (kHeadDim / 8), d8 = i - h * (kHeadDim / 8);
+        __half* o = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim;
+        reinterpret_cast<uint4*>(o)[d8] = val;
+      }
+    }
+  }
+  if (cta >= n) return;
+  const int cbeg = (int)(((long long)cta * total) / n);
+  const int cend = (int)(((long long)(cta + 1) * total) / n);
+  const int npages = cend - cbeg;
+
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
     abort_flag = 0;
@@ -261,11 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
   }
-  const bool segs_in_smem = nseg + 1 <= kSegCache;
-  if (segs_in_smem)
-    for (int i = tid; i <= nseg; i += kThreads) seg_cache[i] = __ldg(&p.seg_start[i]);
   __syncthreads();
-  const int32_t* segs = segs_in_smem ? seg_cache : p.seg_start;
   const int s_first = find_segment(segs, 0, nseg, cbeg);
   volatile int* abort = &abort_flag;
   const uint64_t policy = l2_evict_first_policy();
@@ -295,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       stage_bad[slot] = bad;
       fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
       if (bad) {
+        griddep_wait();  // the planner resets seg_bad and the status word
         atomicOr(&p.seg_bad[sg], 1);
         record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
         mbar_arrive(&full_bar[slot]);
@@ -341,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         poisoned = 1;
         if (lane == 0) {
           *abort = 1;
+          griddep_wait();
           record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
         }
         continue;
@@ -418,7 +521,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             slotp[kMaxGroup * kHeadDim + h] = M;
             slotp[kMaxGroup * kHeadDim + kMaxGroup + h] = L;
           }
-          if (any_poison && tid == 0) atomicOr(&p.seg_bad[s], 1);
+        }
+      }
+      if (!whole) {
+        griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
+        if (any_poison && tid == 0) atomicOr(&p.seg_bad[s], 1);
+        if (p.fused_merge) {
+          // Ticket: the CTA that finishes the segment's last piece merges all
+          // pieces, in slot order, exactly as the combine kernel would.
+          __threadfence();
+          consumer_bar();
+          if (tid == 0) {
+            const int ilo = cta_of_page(sb, total, n), ihi = cta_of_page(se - 1, total, n);
+            merge_last = (atomicAdd(&p.seg_count[s], 1) == ihi - ilo) ? 1 : 0;
+          }
+          consumer_bar();
+          if (merge_last) {
+            __threadfence();
+            merge_pieces(p, s, sb, se, total, n, h, dq);
+          }
         }
       }
     }
@@ -445,8 +566,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const PartialParams& p, int n_max, cudaStream_t stream) {
-  partial_kernel<<<n_max, kThreads, kPartialSmem, stream>>>(tm_k, tm_v, p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: CTAs may start while the planner (the
+  // previous kernel on the stream) still runs; the kernel waits for it with
+  // griddepcontrol.wait before reading or writing anything the planner writes.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_max);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPartialSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, partial_kernel, tm_k, tm_v, p);
 }
 
 cudaError_t set_partial_attributes() {

@@ -9,7 +9,10 @@
 // modes recorded on the page "[Kernel][WIP] Follow up FlashNext batch HC fusion
 // and QSA route audit" (section "Test Result"): a capacity-sized grid with
 // empty CTAs on short contexts, and fixed grids that regress long ones. The
-// plan is computed on the device so the decode step needs no host sync.
+// plan is computed on the device so the decode step needs no host sync. It also
+// resets the status word, the bad-segment flags and the per-segment piece
+// counters of the in-kernel merge; the partial kernel, launched as its
+// programmatic dependent, waits for it before touching any of them.
 #include "xqa_device.cuh"
 #include "xqa_launch.h"
 
@@ -29,10 +32,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             int batch, int num_kv_heads,
                                                             int max_blocks_per_seq, int n_max,
                                                             int min_pages, int32_t* ws) {
+  griddep_launch_dependents();  // the partial kernel may start its prologue now
   const int nseg = batch * num_kv_heads;
   int32_t* header = ws;
   int32_t* seg_start = ws + 4;
   int32_t* seg_bad = seg_start + nseg + 1;
+  int32_t* seg_count = seg_bad + nseg;
   __shared__ int warp_total[kPlanThreads / 32];
   __shared__ int carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -51,11 +56,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       if (bad) record_status(&header[0], XQA_ERR_CTX_TOO_LONG);
       pages = bad ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
       seg_bad[s] = bad ? 1 : 0;
+      seg_count[s] = 0;
     }
     const int incl = warp_inclusive_scan(pages);
     if (lane == 31) warp_total[warp] = incl;
     __syncthreads();
-    if (warp == 0) warp_total[lane] = warp_inclusive_scan(warp_total[lane]);
+    if (warp == 0) {
+      constexpr int kPlanWarps = kPlanThreads / 32;
+      const int t = warp_inclusive_scan(lane < kPlanWarps ? warp_total[lane] : 0);
+      if (lane < kPlanWarps) warp_total[lane] = t;
+    }
     __syncthreads();
     const int excl = carry + incl - pages + (warp > 0 ? warp_total[warp - 1] : 0);
     if (s < nseg) seg_start[s] = excl;
@@ -68,13 +78,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     seg_start[nseg] = total;
     header[2] = total;
     header[3] = nseg;
-    int n = 0;
-    if (total > 0) {
-      const int want = (total + min_pages - 1) / min_pages;
-      n = want < 1 ? 1 : want;
-      n = n < n_max ? n : n_max;
-    }
-    header[1] = n;
+    header[1] = num_ctas_for(total, n_max, min_pages);
   }
 }
 

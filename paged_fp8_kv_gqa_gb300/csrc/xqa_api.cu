@@ -28,7 +28,7 @@ std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
 struct Resolved {
   int batch, hq, hkv, group, mbs, nb;
-  int nseg, n_max, min_pages;
+  int nseg, n_max, min_pages, merge_mode;
   float sm_scale;
   xqa::WsLayout ws;
 };
@@ -44,6 +44,7 @@ xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
   if (group > xqa::kMaxGroup) return XQA_ERR_SHAPE;
   if (s->max_blocks_per_seq < 1 || s->num_blocks < 1) return XQA_ERR_SHAPE;
   if (s->max_ctas < 0 || s->min_pages_per_cta < 0) return XQA_ERR_SHAPE;
+  if (s->merge_mode != 0 && s->merge_mode != 1) return XQA_ERR_SHAPE;
   // int32 index arithmetic on the device: pool rows, total pages, segments
   const long long pool_rows = (long long)s->num_blocks * s->num_kv_heads * kBlockSize;
   const long long max_pages = (long long)s->batch * s->num_kv_heads * s->max_blocks_per_seq;
@@ -58,6 +59,7 @@ xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
   r->nseg = s->batch * s->num_kv_heads;
   r->sm_scale = s->sm_scale > 0.f ? s->sm_scale : (float)(1.0 / sqrt((double)kHeadDim));
   r->min_pages = s->min_pages_per_cta > 0 ? s->min_pages_per_cta : xqa::kDefaultMinPagesPerCta;
+  r->merge_mode = s->merge_mode;
   if (s->max_ctas > 0) {
     r->n_max = s->max_ctas;
   } else {
@@ -167,7 +169,11 @@ xqa_status_t xqa_attend_partial(const void* q, const uint8_t* k_cache, const uin
   p.header = ws_i32(workspace);
   p.seg_start = reinterpret_cast<const int32_t*>(base + r.ws.seg_start_off);
   p.seg_bad = reinterpret_cast<int32_t*>(base + r.ws.seg_bad_off);
+  p.seg_count = reinterpret_cast<int32_t*>(base + r.ws.seg_count_off);
   p.partials = reinterpret_cast<float*>(base + r.ws.partials_off);
+  p.n_max = r.n_max;
+  p.min_pages = r.min_pages;
+  p.fused_merge = r.merge_mode == 0 ? 1 : 0;
   p.batch = r.batch;
   p.num_q_heads = r.hq;
   p.num_kv_heads = r.hkv;
@@ -189,6 +195,7 @@ xqa_status_t xqa_combine(const int32_t* context_lens, float v_scale, void* out,
   if (st != XQA_OK) return st;
   if ((st = check_workspace(r, workspace, workspace_bytes)) != XQA_OK) return st;
   if (!aligned16(out)) return XQA_ERR_ALIGN;
+  if (r.merge_mode == 0) return XQA_OK;  // merged inside the partial kernel
   uint8_t* base = reinterpret_cast<uint8_t*>(workspace);
   xqa::CombineParams p;
   p.out = reinterpret_cast<__half*>(out);

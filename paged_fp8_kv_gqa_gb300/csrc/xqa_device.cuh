@@ -30,7 +30,7 @@ constexpr int kPartialSmem =
     1024 /* alignment slack for the 1024-B swizzle atom */ + kStages * kStageBytes +
     (kScratchFloats + 2 * kWarps * kMaxGroup) * 4 + kSegCache * 4;
 constexpr int kDefaultMinPagesPerCta = 8;
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;  // small enough to share an SM with a partial CTA
 constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
 
 // Partial-result slot: O[8][128] unnormalised fp32, then M[8] (log2 domain), L[8].
@@ -46,6 +46,7 @@ struct WsLayout {
   // header[0] status, [1] num_ctas, [2] total_pages, [3] num_segments
   size_t seg_start_off;  // int32 [nseg + 1]
   size_t seg_bad_off;    // int32 [nseg]
+  size_t seg_count_off;  // int32 [nseg]: pieces finished, for the in-kernel merge
   size_t partials_off;   // float [(n_max + nseg) * kSlotFloats]
   size_t total;
 };
@@ -54,7 +55,8 @@ __host__ __device__ inline WsLayout ws_layout(long long nseg, long long n_max) {
   WsLayout l;
   l.seg_start_off = 16;
   l.seg_bad_off = l.seg_start_off + 4 * (size_t)(nseg + 1);
-  size_t end = l.seg_bad_off + 4 * (size_t)nseg;
+  l.seg_count_off = l.seg_bad_off + 4 * (size_t)nseg;
+  size_t end = l.seg_count_off + 4 * (size_t)nseg;
   l.partials_off = (end + 255) & ~(size_t)255;
   l.total = l.partials_off + (size_t)(n_max + nseg) * kSlotFloats * sizeof(float);
   return l;
@@ -203,6 +205,30 @@ __device__ __forceinline__ uint32_t interleave23(uint32_t x, uint32_t y) { retur
 // From an interleaved word {x_k, x_k+1, y_k, y_k+1}: half2 {x_k, y_k} / {x_k+1, y_k+1}.
 __device__ __forceinline__ uint32_t pair_even(uint32_t iw) { return prmt(iw, 0u, 0x2404u); }
 __device__ __forceinline__ uint32_t pair_odd(uint32_t iw) { return prmt(iw, 0u, 0x3414u); }
+
+// Programmatic dependent launch: the planner lets the partial kernel start
+// early; the partial kernel waits for the planner's writes only where it needs
+// them (no-op when the kernel was not launched as a dependent).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// The planner's split rule (also evaluated inside the partial kernel):
+// n = 0 if P == 0 else min(n_max, max(1, ceil(P / min_pages))).
+__host__ __device__ inline int num_ctas_for(int total_pages, int n_max, int min_pages) {
+  if (total_pages <= 0) return 0;
+  int n = (total_pages + min_pages - 1) / min_pages;
+  n = n < 1 ? 1 : n;
+  return n < n_max ? n : n_max;
+}
+
+// CTA owning flattened page p when P pages are split over n CTAs.
+__host__ __device__ inline int cta_of_page(long long page, long long total, long long n) {
+  return (int)(((page + 1) * n - 1) / total);
+}
 
 __device__ __forceinline__ void record_status(int32_t* status, int code) {
   atomicCAS(status, 0, code);

@@ -15,8 +15,11 @@ struct PartialParams {
   int32_t* header;           // workspace header (status, num_ctas, total_pages, nseg)
   const int32_t* seg_start;  // [nseg + 1]
   int32_t* seg_bad;          // [nseg]
+  int32_t* seg_count;        // [nseg] pieces finished (in-kernel merge tickets)
   float* partials;           // [(n_max + nseg) * kSlotFloats]
   int batch, num_q_heads, num_kv_heads, group, max_blocks_per_seq, num_blocks;
+  int n_max, min_pages;      // split rule inputs (same values the planner got)
+  int fused_merge;           // 1: the last CTA of a split segment merges it
   float scale_log2;  // sm_scale * k_scale * log2(e)
   float v_scale;
 };

@@ -38,14 +38,16 @@ def to_dev(a: np.ndarray) -> torch.Tensor:
 class Dev:
     """A workload's arrays on the GPU plus an output and a workspace."""
 
-    def __init__(self, w: wl.Workload, max_ctas: int = 0, min_pages: int = 0, sm_scale=0.0):
+    def __init__(self, w: wl.Workload, max_ctas: int = 0, min_pages: int = 0, sm_scale=0.0,
+                 merge_mode: int = 0):
         self.w = w
         self.q = to_dev(w.q)
         self.k = to_dev(w.k_cache)
         self.v = to_dev(w.v_cache)
         self.bt = to_dev(w.block_tables)
         self.lens = to_dev(w.context_lens)
-        self.shape = xqa.make_shape(self.q, self.k, self.bt, sm_scale, max_ctas, min_pages)
+        self.shape = xqa.make_shape(self.q, self.k, self.bt, sm_scale, max_ctas, min_pages,
+                                    merge_mode)
         self.out = torch.full_like(self.q, float("nan"))
         self.ws = xqa.alloc_workspace(self.shape)
 

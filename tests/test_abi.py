@@ -52,7 +52,7 @@ def test_host_validation_without_device(lib):
     n = ctypes.c_size_t(0)
     assert lib.xqa_workspace_size(ctypes.byref(shape), ctypes.byref(n)) == xqa.XQA_OK
     nseg = 64
-    head = 16 + 4 * (nseg + 1) + 4 * nseg
+    head = 16 + 4 * (nseg + 1) + 4 * nseg + 4 * nseg
     head = (head + 255) // 256 * 256
     assert n.value == head + (152 + nseg) * (8 * 128 + 16) * 4
     for bad in (
@@ -62,6 +62,7 @@ def test_host_validation_without_device(lib):
         xqa.XqaShape(16, 64, 4, 128, 16, 1200, 22240, 0.0, 152, 0),  # G = 16
         xqa.XqaShape(0, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0),   # batch
         xqa.XqaShape(16, 32, 4, 128, 16, 1200, 2**28, 0.0, 152, 0),  # pool too large for int32 rows
+        xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0, 2),  # merge mode
     ):
         assert lib.xqa_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == xqa.XQA_ERR_SHAPE
     assert lib.xqa_workspace_size(None, ctypes.byref(n)) == xqa.XQA_ERR_NULL

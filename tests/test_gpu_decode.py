@@ -21,11 +21,30 @@ from paged_fp8_kv_gqa_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("merge_mode", [0, 1])
 @pytest.mark.parametrize("name", wl.WORKLOADS)
-def test_workload_matches_oracle(name):
-    out = run(workload(name))
+def test_workload_matches_oracle(name, merge_mode):
+    out = run(workload(name), merge_mode=merge_mode)
     stats = assert_close(out, oracle_out(name), name)
-    print(name, stats)
+    print(name, merge_mode, stats)
+
+
+@pytest.mark.parametrize("name", ["b16_ragged_ctx16384_19200", "b12_boundary"])
+def test_in_kernel_merge_equals_combine_kernel_bitwise(name):
+    a = run(workload(name), merge_mode=0)
+    b = run(workload(name), merge_mode=1)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_large_batch_plan_read_from_planner(merge_mode):
+    # 700 sequences x 4 kv heads: the segment table no longer fits in shared
+    # memory, so the partial kernel reads the planner's table instead
+    rng = np.random.default_rng(77)
+    ctx = rng.integers(0, 120, size=700)
+    ctx[::37] = 0
+    w = wl.make_custom(ctx, 32, 4, seed=77)
+    assert_close(run(w, merge_mode=merge_mode), oracle_of(w), "large batch")
 
 
 @pytest.mark.parametrize("name", ["b4_uniform_ctx1024", "b12_boundary"])
@@ -72,10 +91,11 @@ def test_deterministic():
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
+@pytest.mark.parametrize("merge_mode", [0, 1])
 @pytest.mark.parametrize("max_ctas,min_pages", [(1, 0), (2, 0), (7, 1), (37, 3), (0, 1), (300, 1)])
-def test_split_count_does_not_change_the_result(max_ctas, min_pages):
+def test_split_count_does_not_change_the_result(max_ctas, min_pages, merge_mode):
     name = "b12_boundary"
-    out = run(workload(name), max_ctas=max_ctas, min_pages=min_pages)
+    out = run(workload(name), max_ctas=max_ctas, min_pages=min_pages, merge_mode=merge_mode)
     assert_close(out, oracle_out(name), f"{name} max_ctas={max_ctas}")
 
 
@@ -207,11 +227,12 @@ def test_host_side_errors():
     assert e.value.code == xqa.XQA_ERR_SHAPE
 
 
-def test_bad_block_id_is_reported_and_contained():
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_bad_block_id_is_reported_and_contained(merge_mode):
     w = wl.make_custom([40, 300, 5000], 8, 2, seed=31)
     ref = oracle_of(w)
     w.block_tables[1, 3] = w.num_blocks + 7  # sequence 1 is bad, the others are not
-    d = Dev(w)
+    d = Dev(w, max_ctas=7, merge_mode=merge_mode)  # the bad sequence is split over CTAs
     d.run()
     out = d.result()
     assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
@@ -234,11 +255,12 @@ def test_negative_block_id_is_reported():
     assert np.all(np.isfinite(out[1].astype(np.float32)))
 
 
-def test_context_longer_than_table_is_reported():
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_context_longer_than_table_is_reported(merge_mode):
     w = wl.make_custom([40, 70, 16], 8, 2, seed=33)
     ref = oracle_of(w)
     w.context_lens[1] = w.max_blocks_per_seq * 16 + 1
-    d = Dev(w)
+    d = Dev(w, merge_mode=merge_mode)
     d.run()
     out = d.result()
     assert d.status() == xqa.XQA_ERR_CTX_TOO_LONG
