@@ -231,6 +231,9 @@ def run_gpu(args, world, rank, local, dist):
 
     __graft_entry__.build()
     import paged_fp8_kv_gqa_gb300 as xqa
+
+    if args.lib:  # a differently built libxqa.so with the same ABI (A/B comparisons)
+        xqa.LIB_PATH = os.path.abspath(args.lib)
     from paged_fp8_kv_gqa_gb300 import workloads
 
     torch.cuda.set_device(local)
@@ -537,6 +540,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lib", default="", help="path of an alternative libxqa.so build")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         raise SystemExit("--steps must be >= 1 and --warmup >= 0")

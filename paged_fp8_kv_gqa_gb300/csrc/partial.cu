@@ -277,7 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __shared__ int scan_warp[kWarps];
   __shared__ int scan_carry;
-  __shared__ int merge_last;
+  // split pieces of this CTA (at most its first and last segment), whose
+  // merge tickets are taken once the whole range is done
+  __shared__ int pend_seg[2], pend_poison[2], pend_last[2];
+  __shared__ int npend;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
@@ -411,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
   for (int i = 0; i < kLookahead; ++i) issue_next();
 
+  if (tid == 0) npend = 0;
   WarpState st;
   uint32_t qf[16], qf_next[16];
   int q_next_seg = -1;
@@ -523,29 +527,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!whole) {
-        griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
-        if (any_poison && tid == 0) atomicOr(&p.seg_bad[s], 1);
-        if (p.fused_merge) {
-          // Ticket: the CTA that finishes the segment's last piece merges all
-          // pieces, in slot order, exactly as the combine kernel would.
-          __threadfence();
-          consumer_bar();
-          if (tid == 0) {
-            const int ilo = cta_of_page(sb, total, n), ihi = cta_of_page(se - 1, total, n);
-            merge_last = (atomicAdd(&p.seg_count[s], 1) == ihi - ilo) ? 1 : 0;
-          }
-          consumer_bar();
-          if (merge_last) {
-            __threadfence();
-            merge_pieces(p, s, sb, se, total, n, h, dq);
-          }
-        }
+      if (!whole && tid == 0) {  // a split piece: settle it after the range
+        pend_seg[npend] = s;
+        pend_poison[npend] = any_poison;
+        ++npend;
       }
     }
     consumer_bar();  // scratch is reused by the next segment
     q0 = qe;
     ++s;
+  }
+
+  // ---- split pieces: flag, ticket, and merge by the CTA that finishes last ----
+  // The ticket (a device-wide atomic round trip) is taken once per piece after
+  // the whole range, so no mid-range segment boundary stalls the CTA on it.
+  // The CTA whose ticket completes a segment merges all its pieces in slot
+  // order, exactly as the combine kernel would.
+  if (npend > 0) {
+    griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
+    __threadfence();  // this CTA's partial slots before its tickets
+    consumer_bar();
+    if (tid < npend) {
+      const int s = pend_seg[tid];
+      if (pend_poison[tid]) atomicOr(&p.seg_bad[s], 1);
+      int last = 0;
+      if (p.fused_merge) {
+        const int ilo = cta_of_page(segs[s], total, n), ihi = cta_of_page(segs[s + 1] - 1, total, n);
+        last = (atomicAdd(&p.seg_count[s], 1) == ihi - ilo) ? 1 : 0;
+      }
+      pend_last[tid] = last;
+    }
+    consumer_bar();
+    for (int i = 0; i < npend; ++i) {
+      if (!pend_last[i]) continue;
+      __threadfence();
+      const int s = pend_seg[i];
+      merge_pieces(p, s, segs[s], segs[s + 1], total, n, tid >> 5, (tid & 31) * 4);
+    }
   }
 
   // Drain: after an abort some issued copies may not have been waited for; every
