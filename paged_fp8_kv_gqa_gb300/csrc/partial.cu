@@ -142,21 +142,34 @@ __device__ __forceinline__ void reset_state(WarpState& st) {
   st.m1 = -INFINITY;
 }
 
+// One page's K and V bytes as this lane needs them (see the layout note above).
+struct PageRegs {
+  uint4 ka0, ka1, kb0, kb1;  // K rows g and g+8, dims [32c, 32c+32)
+  uint4 vx, vy, vz, vw;      // V tokens 2c, 2c+1, 2c+8, 2c+9, dims [16g, 16g+16)
+};
+
+// Shared loads of one stage (swizzled 16-byte chunks, conflict-free).
+__device__ __forceinline__ PageRegs load_page(const uint8_t* ks, const uint8_t* vs, int g, int c) {
+  PageRegs r;
+  const int kc0 = ((2 * c) ^ g) << 4, kc1 = ((2 * c + 1) ^ g) << 4;
+  r.ka0 = lds128(ks + g * 128 + kc0);
+  r.ka1 = lds128(ks + g * 128 + kc1);
+  r.kb0 = lds128(ks + (g + 8) * 128 + kc0);
+  r.kb1 = lds128(ks + (g + 8) * 128 + kc1);
+  const int ve = (g ^ (2 * c)) << 4, vo = (g ^ (2 * c + 1)) << 4;
+  r.vx = lds128(vs + (2 * c) * 128 + ve);
+  r.vy = lds128(vs + (2 * c + 1) * 128 + vo);
+  r.vz = lds128(vs + (2 * c + 8) * 128 + ve);
+  r.vw = lds128(vs + (2 * c + 9) * 128 + vo);
+  return r;
+}
+
 // One 16-token page of one kv head: QK, online softmax, PV.
-__device__ __forceinline__ void process_page(WarpState& st, const uint8_t* ks, const uint8_t* vs,
+__device__ __forceinline__ void process_page(WarpState& st, const PageRegs& r,
                                              const uint32_t (&qf)[16], int nvalid, float scale_log2,
                                              int g, int c) {
-  // ---- K and V shared loads (swizzled 16-byte chunks) ----
-  const int kc0 = ((2 * c) ^ g) << 4, kc1 = ((2 * c + 1) ^ g) << 4;
-  const uint4 ka0 = lds128(ks + g * 128 + kc0);
-  const uint4 ka1 = lds128(ks + g * 128 + kc1);
-  const uint4 kb0 = lds128(ks + (g + 8) * 128 + kc0);
-  const uint4 kb1 = lds128(ks + (g + 8) * 128 + kc1);
-  const int ve = (g ^ (2 * c)) << 4, vo = (g ^ (2 * c + 1)) << 4;
-  uint4 vx = lds128(vs + (2 * c) * 128 + ve);
-  uint4 vy = lds128(vs + (2 * c + 1) * 128 + vo);
-  uint4 vz = lds128(vs + (2 * c + 8) * 128 + ve);
-  uint4 vw = lds128(vs + (2 * c + 9) * 128 + vo);
+  const uint4 ka0 = r.ka0, ka1 = r.ka1, kb0 = r.kb0, kb1 = r.kb1;
+  uint4 vx = r.vx, vy = r.vy, vz = r.vz, vw = r.vw;
   if (nvalid < kBlockSize) {  // zero V rows past the context (0 * NaN would poison O)
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     if (2 * c >= nvalid) vx = z;
@@ -244,10 +257,44 @@ __device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int 
     return;
   }
   float M = -INFINITY;
-  for (int i = ilo; i <= ihi; ++i)
-    M = fmaxf(M, __ldcg(p.partials + (size_t)(i + s) * kSlotFloats + kMaxGroup * kHeadDim + h));
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int kFew = 4;
+  if (ihi - ilo < kFew) {
+    // usual case: every load issued before any is used (one L2 round trip)
+    float mi[kFew], li[kFew];
+    float4 oi[kFew];
+#pragma unroll
+    for (int k = 0; k < kFew; ++k) {
+      if (ilo + k <= ihi) {
+        const float* slot = p.partials + (size_t)(ilo + k + s) * kSlotFloats;
+        mi[k] = __ldcg(slot + kMaxGroup * kHeadDim + h);
+        li[k] = __ldcg(slot + kMaxGroup * kHeadDim + kMaxGroup + h);
+        oi[k] = __ldcg(reinterpret_cast<const float4*>(slot + h * kHeadDim + dq));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kFew; ++k)
+      if (ilo + k <= ihi) M = fmaxf(M, mi[k]);
+#pragma unroll
+    for (int k = 0; k < kFew; ++k) {
+      if (ilo + k <= ihi) {
+        const float w = (mi[k] == -INFINITY) ? 0.f : ex2(mi[k] - M);
+        L += w * li[k];
+        acc.x += w * oi[k].x;
+        acc.y += w * oi[k].y;
+        acc.z += w * oi[k].z;
+        acc.w += w * oi[k].w;
+      }
+    }
+    const float r = p.v_scale / L;
+    v.x = pack_half2(acc.x * r, acc.y * r);
+    v.y = pack_half2(acc.z * r, acc.w * r);
+    *reinterpret_cast<uint2*>(o) = v;
+    return;
+  }
+  for (int i = ilo; i <= ihi; ++i)
+    M = fmaxf(M, __ldcg(p.partials + (size_t)(i + s) * kSlotFloats + kMaxGroup * kHeadDim + h));
   for (int i = ilo; i <= ihi; ++i) {
     const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
     const float mi = __ldcg(slot + kMaxGroup * kHeadDim + h);
@@ -452,16 +499,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (stage_bad[slot]) {
+      const uint8_t* stg = stages + slot * kStageBytes;
+      const bool bad_page = stage_bad[slot] != 0;
+      const PageRegs regs = load_page(stg, stg + kPageBytes, g, c);
+      // The page is in registers: refill its slot with page q + kStages right
+      // away (warp-uniform decision), before the math on this page.
+      if (!__any_sync(kFull, *abort != 0)) issue_next();
+      if (bad_page) {
         poisoned = 1;
       } else {
         const int j = cbeg + q - sb;
         const int nvalid = min(kBlockSize, ctx - j * kBlockSize);
-        const uint8_t* stg = stages + slot * kStageBytes;
-        process_page(st, stg, stg + kPageBytes, qf, nvalid, p.scale_log2, g, c);
+        process_page(st, regs, qf, nvalid, p.scale_log2, g, c);
       }
-      // refill the slot just freed with page q + kStages (warp-uniform decision)
-      if (!__any_sync(kFull, *abort != 0)) issue_next();
     }
 
     // ---- merge the 8 warps' states for this segment ----
@@ -545,22 +595,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // order, exactly as the combine kernel would.
   if (npend > 0) {
     griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
-    __threadfence();  // this CTA's partial slots before its tickets
-    consumer_bar();
+    consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
     if (tid < npend) {
       const int s = pend_seg[tid];
       if (pend_poison[tid]) atomicOr(&p.seg_bad[s], 1);
       int last = 0;
       if (p.fused_merge) {
         const int ilo = cta_of_page(segs[s], total, n), ihi = cta_of_page(segs[s + 1] - 1, total, n);
-        last = (atomicAdd(&p.seg_count[s], 1) == ihi - ilo) ? 1 : 0;
+        // release: this CTA's slots (ordered before by the barrier) are visible
+        // to whoever takes a later ticket; acquire: the earlier pieces are
+        // visible to this CTA after the next barrier
+        last = (atom_add_acq_rel_gpu(&p.seg_count[s], 1) == ihi - ilo) ? 1 : 0;
       }
       pend_last[tid] = last;
     }
     consumer_bar();
     for (int i = 0; i < npend; ++i) {
       if (!pend_last[i]) continue;
-      __threadfence();
       const int s = pend_seg[i];
       merge_pieces(p, s, segs[s], segs[s + 1], total, n, tid >> 5, (tid & 31) * 4);
     }

@@ -230,6 +230,14 @@ __host__ __device__ inline int cta_of_page(long long page, long long total, long
   return (int)(((page + 1) * n - 1) / total);
 }
 
+// Device-scope fetch-and-add with acquire-release ordering.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void record_status(int32_t* status, int code) {
   atomicCAS(status, 0, code);
 }
