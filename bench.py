@@ -233,7 +233,9 @@ def run_gpu(args, world, rank, local, dist):
     import paged_fp8_kv_gqa_gb300 as xqa
 
     if args.lib:  # a differently built libxqa.so with the same ABI (A/B comparisons)
+        xqa._lib = None  # build() above loaded the in-tree library
         xqa.LIB_PATH = os.path.abspath(args.lib)
+        xqa.load_library()
     from paged_fp8_kv_gqa_gb300 import workloads
 
     torch.cuda.set_device(local)

@@ -164,38 +164,45 @@ __device__ __forceinline__ PageRegs load_page(const uint8_t* ks, const uint8_t* 
   return r;
 }
 
-// One 16-token page of one kv head: QK, online softmax, PV.
-__device__ __forceinline__ void process_page(WarpState& st, const PageRegs& r,
-                                             const uint32_t (&qf)[16], int nvalid, float scale_log2,
-                                             int g, int c) {
-  const uint4 ka0 = r.ka0, ka1 = r.ka1, kb0 = r.kb0, kb1 = r.kb1;
-  uint4 vx = r.vx, vy = r.vy, vz = r.vz, vw = r.vw;
-  if (nvalid < kBlockSize) {  // zero V rows past the context (0 * NaN would poison O)
-    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    if (2 * c >= nvalid) vx = z;
-    if (2 * c + 1 >= nvalid) vy = z;
-    if (2 * c + 8 >= nvalid) vz = z;
-    if (2 * c + 9 >= nvalid) vw = z;
-  }
-
+// NP (1 or 2) 16-token pages of one kv head: QK, one online-softmax update for
+// all NP pages, PV. With two pages the two independent QK and PV chains
+// interleave, which hides the fixed latencies of one page's chain behind the
+// other's.
+template <int NP>
+__device__ __forceinline__ void process_pages(WarpState& st, const PageRegs (&r)[NP],
+                                              const uint32_t (&qf)[16], const int (&nvalid)[NP],
+                                              float scale_log2, int g, int c) {
   // ---- S^T = K * Q^T : rows tokens (g, g+8), cols heads (2c, 2c+1) ----
-  const uint32_t kr0[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-  const uint32_t kr1[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  float s[NP][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    mma_16816(s, e5m2x2_lo(kr0[j]), e5m2x2_lo(kr1[j]), e5m2x2_hi(kr0[j]), e5m2x2_hi(kr1[j]),
-              qf[2 * j], qf[2 * j + 1]);
+  for (int pi = 0; pi < NP; ++pi) {
+    const uint32_t kr0[8] = {r[pi].ka0.x, r[pi].ka0.y, r[pi].ka0.z, r[pi].ka0.w,
+                             r[pi].ka1.x, r[pi].ka1.y, r[pi].ka1.z, r[pi].ka1.w};
+    const uint32_t kr1[8] = {r[pi].kb0.x, r[pi].kb0.y, r[pi].kb0.z, r[pi].kb0.w,
+                             r[pi].kb1.x, r[pi].kb1.y, r[pi].kb1.z, r[pi].kb1.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[pi][k] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      mma_16816(s[pi], e5m2x2_lo(kr0[j]), e5m2x2_lo(kr1[j]), e5m2x2_hi(kr0[j]),
+                e5m2x2_hi(kr1[j]), qf[2 * j], qf[2 * j + 1]);
+    }
   }
 
-  // ---- online softmax (log2 domain) ----
-  float t0 = s[0] * scale_log2, t1 = s[1] * scale_log2;
-  float t2 = s[2] * scale_log2, t3 = s[3] * scale_log2;
-  if (nvalid < kBlockSize) {
-    if (g >= nvalid) t0 = t1 = -INFINITY;
-    if (g + 8 >= nvalid) t2 = t3 = -INFINITY;
+  // ---- online softmax (log2 domain), one update for all NP pages ----
+  float t[NP][4];
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int pi = 0; pi < NP; ++pi) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) t[pi][k] = s[pi][k] * scale_log2;
+    if (nvalid[pi] < kBlockSize) {
+      if (g >= nvalid[pi]) t[pi][0] = t[pi][1] = -INFINITY;
+      if (g + 8 >= nvalid[pi]) t[pi][2] = t[pi][3] = -INFINITY;
+    }
+    mx0 = fmaxf(mx0, fmaxf(t[pi][0], t[pi][2]));
+    mx1 = fmaxf(mx1, fmaxf(t[pi][1], t[pi][3]));
   }
-  float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
   const bool need = (mx0 > st.m0 + kRescaleThreshold) || (mx1 > st.m1 + kRescaleThreshold);
   if (__any_sync(kFull, need)) {
 #pragma unroll
@@ -219,25 +226,37 @@ __device__ __forceinline__ void process_page(WarpState& st, const PageRegs& r,
     st.l[1] *= a1;
     st.l[3] *= a1;
   }
-  const float p0 = ex2(t0 - st.m0), p1 = ex2(t1 - st.m1);
-  const float p2 = ex2(t2 - st.m0), p3 = ex2(t3 - st.m1);
-  // P^T B-fragments: lane (g, c) gets P[tokens 2c, 2c+1 | 2c+8, 2c+9][head g]
-  const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));
-  const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));
 
-  // ---- O^T += V^T * P^T ----
-  const uint32_t X[4] = {vx.x, vx.y, vx.z, vx.w}, Y[4] = {vy.x, vy.y, vy.z, vy.w};
-  const uint32_t Z[4] = {vz.x, vz.y, vz.z, vz.w}, W[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const uint32_t xy01 = interleave01(X[u], Y[u]), xy23 = interleave23(X[u], Y[u]);
-    const uint32_t zw01 = interleave01(Z[u], W[u]), zw23 = interleave23(Z[u], W[u]);
-    mma_16816(st.o[2 * u], pair_even(xy01), pair_odd(xy01), pair_even(zw01), pair_odd(zw01), pb0,
-              pb1);
-    mma_16816(st.o[2 * u + 1], pair_even(xy23), pair_odd(xy23), pair_even(zw23), pair_odd(zw23),
-              pb0, pb1);
+  for (int pi = 0; pi < NP; ++pi) {
+    const float p0 = ex2(t[pi][0] - st.m0), p1 = ex2(t[pi][1] - st.m1);
+    const float p2 = ex2(t[pi][2] - st.m0), p3 = ex2(t[pi][3] - st.m1);
+    // P^T B-fragments: lane (g, c) gets P[tokens 2c, 2c+1 | 2c+8, 2c+9][head g]
+    const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));
+
+    // ---- O^T += V^T * P^T ----
+    uint4 vx = r[pi].vx, vy = r[pi].vy, vz = r[pi].vz, vw = r[pi].vw;
+    if (nvalid[pi] < kBlockSize) {  // zero V rows past the context (0 * NaN would poison O)
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      if (2 * c >= nvalid[pi]) vx = z;
+      if (2 * c + 1 >= nvalid[pi]) vy = z;
+      if (2 * c + 8 >= nvalid[pi]) vz = z;
+      if (2 * c + 9 >= nvalid[pi]) vw = z;
+    }
+    const uint32_t X[4] = {vx.x, vx.y, vx.z, vx.w}, Y[4] = {vy.x, vy.y, vy.z, vy.w};
+    const uint32_t Z[4] = {vz.x, vz.y, vz.z, vz.w}, W[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t xy01 = interleave01(X[u], Y[u]), xy23 = interleave23(X[u], Y[u]);
+      const uint32_t zw01 = interleave01(Z[u], W[u]), zw23 = interleave23(Z[u], W[u]);
+      mma_16816(st.o[2 * u], pair_even(xy01), pair_odd(xy01), pair_even(zw01), pair_odd(zw01),
+                pb0, pb1);
+      mma_16816(st.o[2 * u + 1], pair_even(xy23), pair_odd(xy23), pair_even(zw23),
+                pair_odd(zw23), pb0, pb1);
+    }
+    mma_16816(st.l, kOnesHalf2, kOnesHalf2, kOnesHalf2, kOnesHalf2, pb0, pb1);
   }
-  mma_16816(st.l, kOnesHalf2, kOnesHalf2, kOnesHalf2, kOnesHalf2, pb0, pb1);
 }
 
 // LSE merge of all pieces of split segment s into fp16 rows (thread: head h,
@@ -487,9 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     reset_state(st);
     int poisoned = 0;
 
-    for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe; q += kWarps) {
-      const int slot = q % kStages;
-      const bool ready = mbar_wait_bounded(&full_bar[slot], (q / kStages) & 1, abort);
+    // this warp's pages of the segment, two at a time (q and q + kWarps)
+    for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe; q += 2 * kWarps) {
+      const bool pair = q + kWarps < qe;
+      const int slot0 = q % kStages, slot1 = (q + kWarps) % kStages;
+      bool ready = mbar_wait_bounded(&full_bar[slot0], (q / kStages) & 1, abort);
+      if (pair) ready = ready && mbar_wait_bounded(&full_bar[slot1], ((q + kWarps) / kStages) & 1, abort);
       if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
         poisoned = 1;
         if (lane == 0) {
@@ -499,18 +521,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const uint8_t* stg = stages + slot * kStageBytes;
-      const bool bad_page = stage_bad[slot] != 0;
-      const PageRegs regs = load_page(stg, stg + kPageBytes, g, c);
-      // The page is in registers: refill its slot with page q + kStages right
-      // away (warp-uniform decision), before the math on this page.
-      if (!__any_sync(kFull, *abort != 0)) issue_next();
-      if (bad_page) {
-        poisoned = 1;
+      const uint8_t* stg0 = stages + slot0 * kStageBytes;
+      const uint8_t* stg1 = stages + slot1 * kStageBytes;
+      const bool bad0 = stage_bad[slot0] != 0, bad1 = pair && stage_bad[slot1] != 0;
+      PageRegs regs[2];
+      regs[0] = load_page(stg0, stg0 + kPageBytes, g, c);
+      if (pair) regs[1] = load_page(stg1, stg1 + kPageBytes, g, c);
+      // The pages are in registers: refill their slots with the pages kStages
+      // ahead right away (warp-uniform decision), before the math.
+      if (!__any_sync(kFull, *abort != 0)) {
+        issue_next();
+        if (pair) issue_next();
+      }
+      const int j0 = cbeg + q - sb;
+      const int nv0 = min(kBlockSize, ctx - j0 * kBlockSize);
+      const int nv1 = min(kBlockSize, ctx - (j0 + kWarps) * kBlockSize);
+      if (pair && !bad0 && !bad1) {
+        const int nv[2] = {nv0, nv1};
+        process_pages<2>(st, regs, qf, nv, p.scale_log2, g, c);
       } else {
-        const int j = cbeg + q - sb;
-        const int nvalid = min(kBlockSize, ctx - j * kBlockSize);
-        process_page(st, regs, qf, nvalid, p.scale_log2, g, c);
+        if (bad0 || bad1) poisoned = 1;
+        if (!bad0) {
+          const PageRegs one[1] = {regs[0]};
+          const int nv[1] = {nv0};
+          process_pages<1>(st, one, qf, nv, p.scale_log2, g, c);
+        }
+        if (pair && !bad1) {
+          const PageRegs one[1] = {regs[1]};
+          const int nv[1] = {nv1};
+          process_pages<1>(st, one, qf, nv, p.scale_log2, g, c);
+        }
       }
     }
 
