@@ -347,6 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // merge tickets are taken once the whole range is done
   __shared__ int pend_seg[2], pend_poison[2], pend_last[2];
   __shared__ int npend;
+  // the segment each merge buffer holds, whether this CTA owns it whole, and
+  // each warp's "met a bad page" flag for it
+  __shared__ int buf_seg[kMergeBufs], buf_whole[kMergeBufs], buf_poison[kMergeBufs][kWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
@@ -354,10 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* scratch = reinterpret_cast<float*>(stages + kStages * kStageBytes);
-  float* scr_m = scratch + kScratchFloats;
-  float* scr_l = scr_m + kWarps * kMaxGroup;
-  int32_t* seg_cache = reinterpret_cast<int32_t*>(scr_l + kWarps * kMaxGroup);
+  float* merge_bufs = reinterpret_cast<float*>(stages + kStages * kStageBytes);
+  int32_t* seg_cache = reinterpret_cast<int32_t*>(merge_bufs + kMergeBufs * kMergeBufFloats);
 
   // ---- the plan: computed here when the segment table fits in shared memory
   // (same integer rule as the planner kernel), else read from the planner ----
@@ -484,6 +485,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   WarpState st;
   uint32_t qf[16], qf_next[16];
   int q_next_seg = -1;
+  // Merge of one buffered segment by all threads (head h, dims dq..dq+3): the
+  // 8 warps' (m, l, O) combine in shared memory; a segment owned whole is
+  // normalised and written as fp16, a split piece goes to partial slot cta + s.
+  auto merge_buffer = [&](int mb) {
+    const int ms = buf_seg[mb];
+    const bool mwhole = buf_whole[mb] != 0;
+    int any_poison = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) any_poison |= buf_poison[mb][w];
+    const float* base = merge_bufs + mb * kMergeBufFloats;
+    const float* bm = base + kScratchFloats;
+    const float* bl = bm + kWarps * kMaxGroup;
+    const int h = tid >> 5;         // 0..7
+    const int dq = (tid & 31) * 4;  // 0..124
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, bm[w * kMaxGroup + h]);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = bm[w * kMaxGroup + h];
+      const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      L += sc * bl[w * kMaxGroup + h];
+      const float4 v =
+          *reinterpret_cast<const float4*>(base + (w * kMaxGroup + h) * kScratchStride + dq);
+      acc.x += sc * v.x;
+      acc.y += sc * v.y;
+      acc.z += sc * v.z;
+      acc.w += sc * v.w;
+    }
+    const int mb_b = ms / p.num_kv_heads, mb_kvh = ms - mb_b * p.num_kv_heads;
+    if (h < p.group) {
+      if (mwhole) {
+        __half* o = p.out +
+                    ((size_t)mb_b * p.num_q_heads + (size_t)mb_kvh * p.group + h) * kHeadDim + dq;
+        const float r = p.v_scale / L;
+        uint2 v;
+        if (any_poison) {
+          const float nan = __int_as_float(0x7fc00000);
+          v.x = pack_half2(nan, nan);
+          v.y = v.x;
+        } else {
+          v.x = pack_half2(acc.x * r, acc.y * r);
+          v.y = pack_half2(acc.z * r, acc.w * r);
+        }
+        *reinterpret_cast<uint2*>(o) = v;
+      } else {
+        float* slotp = p.partials + (size_t)(cta + ms) * kSlotFloats;
+        *reinterpret_cast<float4*>(slotp + h * kHeadDim + dq) = acc;
+        if (dq == 0) {
+          slotp[kMaxGroup * kHeadDim + h] = M;
+          slotp[kMaxGroup * kHeadDim + kMaxGroup + h] = L;
+        }
+      }
+    }
+    if (!mwhole && tid == 0) {  // a split piece: its ticket is taken after the range
+      pend_seg[npend] = ms;
+      pend_poison[npend] = any_poison;
+      ++npend;
+    }
+  };
+
+  int kseg = 0;  // segments of this range finished so far
   int s = s_first;
   int q0 = 0;
   while (q0 < npages) {
@@ -554,9 +619,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    // ---- merge the 8 warps' states for this segment ----
+    // ---- hand this segment's per-warp state to a merge buffer; no CTA-wide
+    // barrier unless the buffer still holds the segment before the previous
+    // one (so a range with at most two segments never stops mid-way) ----
+    const int buf = kseg & 1;
+    if (kseg >= 2) {
+      consumer_bar();
+      merge_buffer(buf);
+      consumer_bar();
+    }
     {
-      float* my = scratch + warp * kMaxGroup * kScratchStride;
+      float* my = merge_bufs + buf * kMergeBufFloats + warp * kMaxGroup * kScratchStride;
+      float* bm = merge_bufs + buf * kMergeBufFloats + kScratchFloats;
+      float* bl = bm + kWarps * kMaxGroup;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int d0 = 16 * g + 2 * i;
@@ -566,67 +641,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         my[(2 * c + 1) * kScratchStride + d0 + 1] = st.o[i][3];
       }
       if (g == 0) {
-        scr_m[warp * kMaxGroup + 2 * c] = st.m0;
-        scr_m[warp * kMaxGroup + 2 * c + 1] = st.m1;
-        scr_l[warp * kMaxGroup + 2 * c] = st.l[0];
-        scr_l[warp * kMaxGroup + 2 * c + 1] = st.l[1];
+        bm[warp * kMaxGroup + 2 * c] = st.m0;
+        bm[warp * kMaxGroup + 2 * c + 1] = st.m1;
+        bl[warp * kMaxGroup + 2 * c] = st.l[0];
+        bl[warp * kMaxGroup + 2 * c + 1] = st.l[1];
+      }
+      if (lane == 0) buf_poison[buf][warp] = poisoned;
+      if (tid == 0) {
+        buf_seg[buf] = s;
+        buf_whole[buf] = whole ? 1 : 0;
       }
     }
-    const int any_poison = consumer_bar_or(poisoned);
-    {
-      const int h = tid >> 5;          // 0..7
-      const int dq = (tid & 31) * 4;   // 0..124
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, scr_m[w * kMaxGroup + h]);
-      float L = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = scr_m[w * kMaxGroup + h];
-        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        L += sc * scr_l[w * kMaxGroup + h];
-        const float4 v =
-            *reinterpret_cast<const float4*>(scratch + (w * kMaxGroup + h) * kScratchStride + dq);
-        acc.x += sc * v.x;
-        acc.y += sc * v.y;
-        acc.z += sc * v.z;
-        acc.w += sc * v.w;
-      }
-      if (h < p.group) {
-        if (whole) {
-          __half* o = p.out +
-                      ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim + dq;
-          const float r = p.v_scale / L;
-          uint2 v;
-          if (any_poison) {
-            const float nan = __int_as_float(0x7fc00000);
-            v.x = pack_half2(nan, nan);
-            v.y = v.x;
-          } else {
-            v.x = pack_half2(acc.x * r, acc.y * r);
-            v.y = pack_half2(acc.z * r, acc.w * r);
-          }
-          *reinterpret_cast<uint2*>(o) = v;
-        } else {
-          float* slotp = p.partials + (size_t)(cta + s) * kSlotFloats;
-          *reinterpret_cast<float4*>(slotp + h * kHeadDim + dq) = acc;
-          if (dq == 0) {
-            slotp[kMaxGroup * kHeadDim + h] = M;
-            slotp[kMaxGroup * kHeadDim + kMaxGroup + h] = L;
-          }
-        }
-      }
-      if (!whole && tid == 0) {  // a split piece: settle it after the range
-        pend_seg[npend] = s;
-        pend_poison[npend] = any_poison;
-        ++npend;
-      }
-    }
-    consumer_bar();  // scratch is reused by the next segment
+    ++kseg;
     q0 = qe;
     ++s;
   }
+
+  // ---- merges still buffered (the range's last one or two segments) ----
+  consumer_bar();
+  if (kseg >= 2) merge_buffer(kseg & 1);
+  if (kseg >= 1) merge_buffer((kseg - 1) & 1);
+  consumer_bar();
 
   // ---- split pieces: flag, ticket, and merge by the CTA that finishes last ----
   // The ticket (a device-wide atomic round trip) is taken once per piece after

@@ -25,10 +25,13 @@ constexpr int kStages = 32;                                   // smem ring depth
 constexpr int kLookahead = kStages / kWarps;                  // pages in flight per warp
 constexpr int kScratchStride = kHeadDim + 4;                  // floats per (warp, head) merge row
 constexpr int kScratchFloats = kWarps * kMaxGroup * kScratchStride;
+// one merge buffer: every warp's O rows, then m[warp][head], l[warp][head]
+constexpr int kMergeBufFloats = kScratchFloats + 2 * kWarps * kMaxGroup;
+constexpr int kMergeBufs = 2;  // segments whose merge may be pending at once
 constexpr int kSegCache = 2048;                               // seg_start entries kept in smem
 constexpr int kPartialSmem =
     1024 /* alignment slack for the 1024-B swizzle atom */ + kStages * kStageBytes +
-    (kScratchFloats + 2 * kWarps * kMaxGroup) * 4 + kSegCache * 4;
+    kMergeBufs * kMergeBufFloats * 4 + kSegCache * 4;
 constexpr int kDefaultMinPagesPerCta = 8;
 constexpr int kPlanThreads = 256;  // small enough to share an SM with a partial CTA
 constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
