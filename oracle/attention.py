@@ -10,8 +10,10 @@ The pages print no formula, so the following readings are taken:
 
 * q head ``h`` reads kv head ``h // G`` with ``G = Hq / Hkv`` (consecutive groups);
 * logical token ``t`` of sequence ``b`` lives in physical page
-  ``block_tables[b, t // BS]``, slot ``t % BS``; cache layout [NB, Hkv, BS, D];
-* ``k = k_scale * decode(K code)``, ``v = v_scale * decode(V code)``;
+  ``block_tables[b, t // BS]``, slot ``t % BS``; cache layout [NB, Hkv, BS, D]
+  ("hnd", the default) or [NB, BS, Hkv, D] ("nhd");
+* ``k = k_scale * decode(K code)``, ``v = v_scale * decode(V code)`` with the
+  E5M2 decode (default) or the E4M3 decode;
 * ``s_t = sm_scale * <q, k_t>`` with ``sm_scale = 1/sqrt(D)`` unless given;
 * ``out = sum_t softmax(s)_t v_t`` over ``t < ctx_b`` only (tokens past the
   context are never read); ``ctx_b == 0`` gives a zero output row.
@@ -25,17 +27,34 @@ import math
 
 import numpy as np
 
-from . import e5m2
+from . import e4m3, e5m2
 
 
-def gather_sequence_kv(cache: np.ndarray, block_tables: np.ndarray, b: int, ctx: int, kv_head: int) -> np.ndarray:
+def code_table(kv_dtype: str) -> np.ndarray:
+    """float64 value of all 256 codes of the KV format."""
+    if kv_dtype == "e5m2":
+        return e5m2.lut()
+    if kv_dtype == "e4m3":
+        return e4m3.lut()
+    raise ValueError(kv_dtype)
+
+
+def gather_sequence_kv(cache: np.ndarray, block_tables: np.ndarray, b: int, ctx: int, kv_head: int,
+                       kv_layout: str = "hnd") -> np.ndarray:
     """Codes of tokens 0..ctx-1 of sequence ``b``, kv head ``kv_head``: uint8 [ctx, D]."""
-    num_blocks, _, bs, d = cache.shape
+    if kv_layout == "hnd":
+        num_blocks, _, bs, d = cache.shape
+    elif kv_layout == "nhd":
+        num_blocks, bs, _, d = cache.shape
+    else:
+        raise ValueError(kv_layout)
     npages = (ctx + bs - 1) // bs
     pages = np.asarray(block_tables[b, :npages], dtype=np.int64)
     if np.any(pages < 0) or np.any(pages >= num_blocks):
         raise ValueError(f"sequence {b}: block id out of range in the first {npages} table entries")
-    return cache[pages, kv_head].reshape(npages * bs, d)[:ctx]
+    if kv_layout == "hnd":
+        return cache[pages, kv_head].reshape(npages * bs, d)[:ctx]
+    return cache[pages, :, kv_head].reshape(npages * bs, d)[:ctx]
 
 
 def paged_decode_attention(
@@ -47,16 +66,19 @@ def paged_decode_attention(
     k_scale: float,
     v_scale: float,
     sm_scale: float | None = None,
+    kv_dtype: str = "e5m2",
+    kv_layout: str = "hnd",
 ) -> np.ndarray:
     """One decode step: float64 [B, Hq, D] attention output."""
     batch, hq, d = q.shape
-    _, hkv, _, d2 = k_cache.shape
+    hkv = k_cache.shape[1] if kv_layout == "hnd" else k_cache.shape[2]
+    d2 = k_cache.shape[3]
     if d2 != d or hq % hkv != 0:
         raise ValueError("shape mismatch")
     group = hq // hkv
     if sm_scale is None or sm_scale <= 0.0:
         sm_scale = 1.0 / math.sqrt(d)
-    table = e5m2.lut()
+    table = code_table(kv_dtype)
     out = np.zeros((batch, hq, d), dtype=np.float64)
     for b in range(batch):
         ctx = int(context_lens[b])
@@ -65,8 +87,8 @@ def paged_decode_attention(
         if ctx == 0:
             continue
         for g in range(hkv):
-            k = float(k_scale) * table[gather_sequence_kv(k_cache, block_tables, b, ctx, g)]
-            v = float(v_scale) * table[gather_sequence_kv(v_cache, block_tables, b, ctx, g)]
+            k = float(k_scale) * table[gather_sequence_kv(k_cache, block_tables, b, ctx, g, kv_layout)]
+            v = float(v_scale) * table[gather_sequence_kv(v_cache, block_tables, b, ctx, g, kv_layout)]
             heads = slice(g * group, (g + 1) * group)
             qh = q[b, heads].astype(np.float64)
             s = float(sm_scale) * (qh @ k.T)  # [G, ctx]
@@ -87,22 +109,24 @@ def paged_decode_attention_rows(
     v_scale: float,
     rows,
     sm_scale: float | None = None,
+    kv_dtype: str = "e5m2",
+    kv_layout: str = "hnd",
 ) -> np.ndarray:
     """The same definition evaluated for selected (b, h) rows only: float64 [len(rows), D]."""
     batch, hq, d = q.shape
-    hkv = k_cache.shape[1]
+    hkv = k_cache.shape[1] if kv_layout == "hnd" else k_cache.shape[2]
     group = hq // hkv
     if sm_scale is None or sm_scale <= 0.0:
         sm_scale = 1.0 / math.sqrt(d)
-    table = e5m2.lut()
+    table = code_table(kv_dtype)
     res = np.zeros((len(rows), d), dtype=np.float64)
     for i, (b, h) in enumerate(rows):
         ctx = int(context_lens[b])
         if ctx == 0:
             continue
         g = h // group
-        k = float(k_scale) * table[gather_sequence_kv(k_cache, block_tables, b, ctx, g)]
-        v = float(v_scale) * table[gather_sequence_kv(v_cache, block_tables, b, ctx, g)]
+        k = float(k_scale) * table[gather_sequence_kv(k_cache, block_tables, b, ctx, g, kv_layout)]
+        v = float(v_scale) * table[gather_sequence_kv(v_cache, block_tables, b, ctx, g, kv_layout)]
         s = float(sm_scale) * (k @ q[b, h].astype(np.float64))
         s = s - s.max()
         p = np.exp(s)

@@ -25,6 +25,7 @@ import pytest
 import torch
 
 import oracle.attention as attn
+import oracle.e4m3 as e4m3_mod
 import oracle.e5m2 as e5m2_mod
 from paged_fp8_kv_gqa_gb300 import workloads as wl
 
@@ -274,7 +275,8 @@ def _mutant(old, new):
     mod = types.ModuleType("oracle_mutant")
     mod.__dict__["__name__"] = "oracle_mutant"
     mod.__dict__["e5m2"] = e5m2_mod
-    code = src.replace("from . import e5m2", "")
+    mod.__dict__["e4m3"] = e4m3_mod
+    code = src.replace("from . import e4m3, e5m2", "")
     exec(compile(code.replace(old, new), "oracle_mutant", "exec"), mod.__dict__)
     return mod.paged_decode_attention
 
