@@ -53,6 +53,14 @@ typedef enum xqa_status {
   XQA_ERR_DEVICE_TIMEOUT = 18   /* a pipeline wait exceeded its time budget */
 } xqa_status_t;
 
+/* KV cache code formats (xqa_shape_t.kv_dtype). */
+#define XQA_KV_E5M2 0 /* 1 sign, 5 exponent (bias 15), 2 mantissa bits */
+#define XQA_KV_E4M3 1 /* 1 sign, 4 exponent (bias 7), 3 mantissa bits, no inf */
+
+/* KV cache layouts (xqa_shape_t.kv_layout). */
+#define XQA_LAYOUT_HND 0 /* [NB, Hkv, BS, D]: one (page, kv head) slice is contiguous */
+#define XQA_LAYOUT_NHD 1 /* [NB, BS, Hkv, D]: token-major pages */
+
 /* Problem dimensions. head_dim must be 128 and block_size 16; Hq must be a
  * multiple of Hkv with G = Hq / Hkv <= 8. */
 typedef struct xqa_shape {
@@ -70,6 +78,8 @@ typedef struct xqa_shape {
                                  0 = by the last CTA to finish one (inside the
                                  partial kernel, default); 1 = by the separate
                                  combine kernel (xqa_combine) */
+  int32_t kv_dtype;           /* XQA_KV_E5M2 (0, default) or XQA_KV_E4M3 */
+  int32_t kv_layout;          /* XQA_LAYOUT_HND (0, default) or XQA_LAYOUT_NHD */
 } xqa_shape_t;
 
 /* Bytes of device workspace xqa_decode needs for `shape` on the current
@@ -79,14 +89,16 @@ xqa_status_t xqa_workspace_size(const xqa_shape_t* shape, size_t* bytes);
 /* One decode step of paged GQA attention.
  *
  *   q             device, fp16 [B, Hq, D], contiguous, 16-byte aligned
- *   k_cache       device, E5M2 bytes [NB, Hkv, BS, D] (one (page, kv head)
- *                 slice is BS*D = 2048 contiguous bytes), 16-byte aligned
+ *   k_cache       device, FP8 codes (shape->kv_dtype) in the shape->kv_layout
+ *                 layout: [NB, Hkv, BS, D] (HND: one (page, kv head) slice is
+ *                 BS*D = 2048 contiguous bytes) or [NB, BS, Hkv, D] (NHD),
+ *                 16-byte aligned
  *   v_cache       device, same layout as k_cache
  *   block_tables  device, int32 [B, MBS]; entry j of row b is the physical page
  *                 of tokens [16j, 16j+16) of sequence b; entries at or past
  *                 ceil(ctx_b / 16) are never read
  *   context_lens  device, int32 [B]; 0 <= ctx_b <= MBS*BS (0 gives a zero row)
- *   k_scale       per-tensor K scale (the key value is k_scale * E5M2(code))
+ *   k_scale       per-tensor K scale (the key value is k_scale * FP8(code))
  *   v_scale       per-tensor V scale
  *   out           device, fp16 [B, Hq, D], contiguous, 16-byte aligned
  *   workspace     device, >= xqa_workspace_size bytes, 256-byte aligned; holds
@@ -103,6 +115,16 @@ xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_
                         const int32_t* block_tables, const int32_t* context_lens,
                         float k_scale, float v_scale, void* out, const xqa_shape_t* shape,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* xqa_decode with the per-tensor scales read from device memory when the
+ * kernels run (so a captured CUDA graph picks up new scales on replay):
+ * k_scale and v_scale are device pointers to one float each. Results are
+ * bitwise equal to xqa_decode called with the same values. */
+xqa_status_t xqa_decode_device_scales(const void* q, const uint8_t* k_cache,
+                                      const uint8_t* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, const float* k_scale,
+                                      const float* v_scale, void* out, const xqa_shape_t* shape,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* The three stages of xqa_decode, exposed separately so they can be timed one
  * by one. Called in this order with the same arguments they are exactly
@@ -127,6 +149,14 @@ xqa_status_t xqa_combine(const int32_t* context_lens, float v_scale, void* out,
  * in, out_fp16_bits, out_f32: device pointers, n elements each; any
  * alignment. */
 xqa_status_t xqa_dequant_e5m2(const uint8_t* in, size_t n, float scale, uint16_t* out_fp16_bits,
+                              float* out_f32, void* stream);
+
+/* Exact E4M3 dequantisation with the conversion routes the attention kernel
+ * uses for E4M3 caches (every E4M3 value is an fp16 value):
+ *   out_fp16_bits[i] = fp16 pattern of E4M3(in[i])      (exact; NaN codes -> NaN)
+ *   out_f32[i]       = (float)fp16 * scale              (optional; NULL to skip)
+ * Same argument conventions as xqa_dequant_e5m2. */
+xqa_status_t xqa_dequant_e4m3(const uint8_t* in, size_t n, float scale, uint16_t* out_fp16_bits,
                               float* out_f32, void* stream);
 
 /* Copies the workspace status word to *device_status (an xqa_status_t value:

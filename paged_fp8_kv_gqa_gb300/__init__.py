@@ -7,8 +7,9 @@ these functions raise.
 
 The names mirror the C ABI declared in ``include/xqa.h``:
 ``xqa_workspace_size``, ``xqa_decode``, ``xqa_plan``, ``xqa_attend_partial``,
-``xqa_combine``, ``xqa_dequant_e5m2``, ``xqa_read_status``, ``xqa_read_plan``,
-``xqa_status_string``.
+``xqa_combine``, ``xqa_decode_device_scales``, ``xqa_dequant_e5m2``,
+``xqa_dequant_e4m3``, ``xqa_read_status``, ``xqa_read_plan``, ``xqa_status_string``,
+``xqa_decode_static_workspace``.
 """
 from __future__ import annotations
 
@@ -42,7 +43,12 @@ EXPORTED = (
     "xqa_read_plan",
     "xqa_status_string",
     "xqa_decode_static_workspace",
+    "xqa_decode_device_scales",
+    "xqa_dequant_e4m3",
 )
+
+KV_DTYPES = {"e5m2": 0, "e4m3": 1}
+KV_LAYOUTS = {"hnd": 0, "nhd": 1}
 
 
 class XqaShape(ctypes.Structure):
@@ -60,6 +66,8 @@ class XqaShape(ctypes.Structure):
         ("max_ctas", ctypes.c_int32),
         ("min_pages_per_cta", ctypes.c_int32),
         ("merge_mode", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("kv_layout", ctypes.c_int32),
     ]
 
 
@@ -86,6 +94,8 @@ _SIGS = {
     "xqa_read_plan": [_P, _SHAPE, _P, _P, _P, _P],
     "xqa_status_string": [ctypes.c_int],
     "xqa_decode_static_workspace": [_P, _P, _P, _P, _P, _F, _F, _P, _SHAPE, _P],
+    "xqa_decode_device_scales": [_P, _P, _P, _P, _P, _P, _P, _P, _SHAPE, _P, _SZ, _P],
+    "xqa_dequant_e4m3": [_P, _SZ, _F, _P, _P, _P],
 }
 
 
@@ -134,15 +144,19 @@ def _cuda(t: torch.Tensor, dtype, name: str) -> int:
 
 def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
                sm_scale: float = 0.0, max_ctas: int = 0, min_pages_per_cta: int = 0,
-               merge_mode: int = 0) -> XqaShape:
-    """Shape descriptor from q [B, Hq, D], k_cache [NB, Hkv, BS, D], block_tables [B, MBS]."""
+               merge_mode: int = 0, kv_dtype: str = "e5m2", kv_layout: str = "hnd") -> XqaShape:
+    """Shape descriptor from q [B, Hq, D], block_tables [B, MBS] and k_cache
+    [NB, Hkv, BS, D] (kv_layout "hnd") or [NB, BS, Hkv, D] ("nhd")."""
     b, hq, d = q.shape
-    nb, hkv, bs, d2 = k_cache.shape
+    if kv_layout == "hnd":
+        nb, hkv, bs, d2 = k_cache.shape
+    else:
+        nb, bs, hkv, d2 = k_cache.shape
     if d2 != d or block_tables.shape[0] != b:
         raise ValueError("inconsistent q / k_cache / block_tables shapes")
     return XqaShape(int(b), int(hq), int(hkv), int(d), int(bs), int(block_tables.shape[1]),
                     int(nb), float(sm_scale), int(max_ctas), int(min_pages_per_cta),
-                    int(merge_mode))
+                    int(merge_mode), KV_DTYPES[kv_dtype], KV_LAYOUTS[kv_layout])
 
 
 def xqa_workspace_size(shape: XqaShape) -> int:
@@ -169,21 +183,34 @@ def _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace
     )
 
 
-def xqa_decode(q, k_cache, v_cache, block_tables, context_lens, k_scale: float, v_scale: float,
+def xqa_decode(q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale,
                out=None, workspace=None, shape: XqaShape | None = None, stream=None,
-               sm_scale: float = 0.0, max_ctas: int = 0, min_pages_per_cta: int = 0):
-    """One decode step. Tensors: q fp16 [B,Hq,D]; k/v_cache uint8 E5M2 [NB,Hkv,16,D];
-    block_tables int32 [B,MBS]; context_lens int32 [B]. Returns ``out`` fp16 [B,Hq,D]."""
+               sm_scale: float = 0.0, max_ctas: int = 0, min_pages_per_cta: int = 0,
+               kv_dtype: str = "e5m2", kv_layout: str = "hnd"):
+    """One decode step. Tensors: q fp16 [B,Hq,D]; k/v_cache uint8 FP8 codes
+    [NB,Hkv,16,D] (or [NB,16,Hkv,D] for kv_layout "nhd"); block_tables int32
+    [B,MBS]; context_lens int32 [B]. k_scale / v_scale are floats, or float32
+    CUDA tensors of one element (read on the device: xqa_decode_device_scales).
+    Returns ``out`` fp16 [B,Hq,D]."""
     if shape is None:
-        shape = make_shape(q, k_cache, block_tables, sm_scale, max_ctas, min_pages_per_cta)
+        shape = make_shape(q, k_cache, block_tables, sm_scale, max_ctas, min_pages_per_cta,
+                           kv_dtype=kv_dtype, kv_layout=kv_layout)
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
         workspace = alloc_workspace(shape, q.device)
     a = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace, shape)
-    _check(load_library().xqa_decode(a[0], a[1], a[2], a[3], a[4], float(k_scale), float(v_scale),
-                                     a[5], ctypes.byref(shape), a[6], workspace.numel(),
-                                     _stream_handle(stream)), "xqa_decode")
+    lib = load_library()
+    if isinstance(k_scale, torch.Tensor) or isinstance(v_scale, torch.Tensor):
+        ks = _cuda(k_scale, torch.float32, "k_scale")
+        vs = _cuda(v_scale, torch.float32, "v_scale")
+        _check(lib.xqa_decode_device_scales(a[0], a[1], a[2], a[3], a[4], ks, vs, a[5],
+                                            ctypes.byref(shape), a[6], workspace.numel(),
+                                            _stream_handle(stream)), "xqa_decode_device_scales")
+        return out
+    _check(lib.xqa_decode(a[0], a[1], a[2], a[3], a[4], float(k_scale), float(v_scale), a[5],
+                          ctypes.byref(shape), a[6], workspace.numel(), _stream_handle(stream)),
+           "xqa_decode")
     return out
 
 
@@ -210,16 +237,24 @@ def xqa_combine(context_lens, v_scale, out, workspace, shape: XqaShape, stream=N
                                       workspace.numel(), _stream_handle(stream)), "xqa_combine")
 
 
-def xqa_dequant_e5m2(codes: torch.Tensor, scale: float = 1.0, with_f32: bool = True, stream=None):
-    """Exact dequantisation: returns (fp16 bit patterns as int16 tensor, fp32 scaled or None)."""
+def _dequant(fn_name, codes, scale, with_f32, stream):
     n = codes.numel()
     out16 = torch.empty(n, dtype=torch.int16, device=codes.device)
     out32 = torch.empty(n, dtype=torch.float32, device=codes.device) if with_f32 else None
-    _check(load_library().xqa_dequant_e5m2(
+    _check(getattr(load_library(), fn_name)(
         _cuda(codes, torch.uint8, "codes"), n, float(scale), out16.data_ptr(),
-        out32.data_ptr() if out32 is not None else None, _stream_handle(stream)),
-        "xqa_dequant_e5m2")
+        out32.data_ptr() if out32 is not None else None, _stream_handle(stream)), fn_name)
     return out16, out32
+
+
+def xqa_dequant_e5m2(codes: torch.Tensor, scale: float = 1.0, with_f32: bool = True, stream=None):
+    """Exact dequantisation: returns (fp16 bit patterns as int16 tensor, fp32 scaled or None)."""
+    return _dequant("xqa_dequant_e5m2", codes, scale, with_f32, stream)
+
+
+def xqa_dequant_e4m3(codes: torch.Tensor, scale: float = 1.0, with_f32: bool = True, stream=None):
+    """Exact E4M3 dequantisation: (fp16 bit patterns as int16 tensor, fp32 scaled or None)."""
+    return _dequant("xqa_dequant_e4m3", codes, scale, with_f32, stream)
 
 
 def xqa_read_status(workspace: torch.Tensor, stream=None) -> int:

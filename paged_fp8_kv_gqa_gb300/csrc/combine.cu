@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
     acc.z += w * v.z;
     acc.w += w * v.w;
   }
-  const float r = p.v_scale / L;
+  const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
+  const float r = v_scale / L;
   store_half4(o, acc.x * r, acc.y * r, acc.z * r, acc.w * r);
 }
 

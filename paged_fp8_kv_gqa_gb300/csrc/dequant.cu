@@ -5,12 +5,14 @@
 // route used for K, odd groups the "same byte of two words" route used for V,
 // so a test over all 256 codes at both parities checks both routes bit for bit.
 // This is the "E5M2 conversion" phase named on the page "[Kernel][SM70]
-// Pipeline batched E5M2 XQA decode" (section "Pending work and gates").
+// Pipeline batched E5M2 XQA decode" (section "Pending work and gates"), and
+// its E4M3 counterpart.
 #include "xqa_device.cuh"
 #include "xqa_launch.h"
 
 namespace xqa {
 
+template <int kFmt>
 __global__ void dequant_kernel(const uint8_t* __restrict__ in, size_t n, float scale,
                                uint16_t* __restrict__ out16, float* __restrict__ out32) {
   const size_t ngroups = (n + 7) / 8;
@@ -25,15 +27,16 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ in, size_t n, float s
     }
     uint16_t h[8];
     if ((grp & 1) == 0) {
-      const uint32_t r[4] = {e5m2x2_lo(x), e5m2x2_hi(x), e5m2x2_lo(y), e5m2x2_hi(y)};
+      const uint32_t r[4] = {KvConv<kFmt>::k_lo(x), KvConv<kFmt>::k_hi(x), KvConv<kFmt>::k_lo(y),
+                             KvConv<kFmt>::k_hi(y)};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         h[2 * k] = (uint16_t)(r[k] & 0xffffu);
         h[2 * k + 1] = (uint16_t)(r[k] >> 16);
       }
     } else {
-      const uint32_t i01 = interleave01(x, y), i23 = interleave23(x, y);
-      const uint32_t r[4] = {pair_even(i01), pair_odd(i01), pair_even(i23), pair_odd(i23)};
+      uint32_t r[4];
+      KvConv<kFmt>::v_pairs(x, y, r);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {  // r[k] = {x_k, y_k}
         h[k] = (uint16_t)(r[k] & 0xffffu);
@@ -50,13 +53,16 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ in, size_t n, float s
   }
 }
 
-cudaError_t launch_dequant(const uint8_t* in, size_t n, float scale, uint16_t* out16,
-                           float* out32, cudaStream_t stream) {
+cudaError_t launch_dequant(int kv_dtype, const uint8_t* in, size_t n, float scale,
+                           uint16_t* out16, float* out32, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
   const size_t ngroups = (n + 7) / 8;
   size_t blocks = (ngroups + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  dequant_kernel<<<(unsigned)blocks, 256, 0, stream>>>(in, n, scale, out16, out32);
+  if (kv_dtype == XQA_KV_E4M3)
+    dequant_kernel<XQA_KV_E4M3><<<(unsigned)blocks, 256, 0, stream>>>(in, n, scale, out16, out32);
+  else
+    dequant_kernel<XQA_KV_E5M2><<<(unsigned)blocks, 256, 0, stream>>>(in, n, scale, out16, out32);
   return cudaGetLastError();
 }
 

@@ -98,7 +98,8 @@ __device__ __forceinline__ PageBatch load_batch(const PartialParams& p, const in
     const int j = pg - segs[s];
     const int id = __ldg(&p.block_tables[(size_t)b * p.max_blocks_per_seq + j]);
     r.bad = (id < 0 || id >= p.num_blocks) ? 1 : 0;
-    r.y = r.bad ? 0 : (id * p.num_kv_heads + kvh) * kBlockSize;
+    // HND: row of the (page, kv head) slice; NHD: first token row of the page
+    r.y = r.bad ? 0 : (p.kv_layout == XQA_LAYOUT_HND ? (id * p.num_kv_heads + kvh) : id) * kBlockSize;
     r.seg = s;
   }
   return r;
@@ -168,7 +169,7 @@ __device__ __forceinline__ PageRegs load_page(const uint8_t* ks, const uint8_t* 
 // all NP pages, PV. With two pages the two independent QK and PV chains
 // interleave, which hides the fixed latencies of one page's chain behind the
 // other's.
-template <int NP>
+template <int kFmt, int NP>
 __device__ __forceinline__ void process_pages(WarpState& st, const PageRegs (&r)[NP],
                                               const uint32_t (&qf)[16], const int (&nvalid)[NP],
                                               float scale_log2, int g, int c) {
@@ -184,8 +185,9 @@ __device__ __forceinline__ void process_pages(WarpState& st, const PageRegs (&r)
     for (int k = 0; k < 4; ++k) s[pi][k] = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      mma_16816(s[pi], e5m2x2_lo(kr0[j]), e5m2x2_lo(kr1[j]), e5m2x2_hi(kr0[j]),
-                e5m2x2_hi(kr1[j]), qf[2 * j], qf[2 * j + 1]);
+      mma_16816(s[pi], KvConv<kFmt>::k_lo(kr0[j]), KvConv<kFmt>::k_lo(kr1[j]),
+                KvConv<kFmt>::k_hi(kr0[j]), KvConv<kFmt>::k_hi(kr1[j]), qf[2 * j],
+                qf[2 * j + 1]);
     }
   }
 
@@ -248,12 +250,11 @@ __device__ __forceinline__ void process_pages(WarpState& st, const PageRegs (&r)
     const uint32_t Z[4] = {vz.x, vz.y, vz.z, vz.w}, W[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const uint32_t xy01 = interleave01(X[u], Y[u]), xy23 = interleave23(X[u], Y[u]);
-      const uint32_t zw01 = interleave01(Z[u], W[u]), zw23 = interleave23(Z[u], W[u]);
-      mma_16816(st.o[2 * u], pair_even(xy01), pair_odd(xy01), pair_even(zw01), pair_odd(zw01),
-                pb0, pb1);
-      mma_16816(st.o[2 * u + 1], pair_even(xy23), pair_odd(xy23), pair_even(zw23),
-                pair_odd(zw23), pb0, pb1);
+      uint32_t xy[4], zw[4];  // {x_k, y_k}: tokens 2c, 2c+1 / 2c+8, 2c+9 at dim byte k
+      KvConv<kFmt>::v_pairs(X[u], Y[u], xy);
+      KvConv<kFmt>::v_pairs(Z[u], W[u], zw);
+      mma_16816(st.o[2 * u], xy[0], xy[1], zw[0], zw[1], pb0, pb1);
+      mma_16816(st.o[2 * u + 1], xy[2], xy[3], zw[2], zw[3], pb0, pb1);
     }
     mma_16816(st.l, kOnesHalf2, kOnesHalf2, kOnesHalf2, kOnesHalf2, pb0, pb1);
   }
@@ -262,7 +263,7 @@ __device__ __forceinline__ void process_pages(WarpState& st, const PageRegs (&r)
 // LSE merge of all pieces of split segment s into fp16 rows (thread: head h,
 // dims dq..dq+3). Pieces were written by other CTAs: read through L2.
 __device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int sb, int se,
-                                             int total, int n, int h, int dq) {
+                                             int total, int n, int h, int dq, float v_scale) {
   if (h >= p.group) return;
   const int ilo = cta_of_page(sb, total, n), ihi = cta_of_page(se - 1, total, n);
   const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
@@ -306,7 +307,7 @@ __device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int 
         acc.w += w * oi[k].w;
       }
     }
-    const float r = p.v_scale / L;
+    const float r = v_scale / L;
     v.x = pack_half2(acc.x * r, acc.y * r);
     v.y = pack_half2(acc.z * r, acc.w * r);
     *reinterpret_cast<uint2*>(o) = v;
@@ -325,7 +326,7 @@ __device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int 
     acc.z += w * x.z;
     acc.w += w * x.w;
   }
-  const float r = p.v_scale / L;
+  const float r = v_scale / L;
   v.x = pack_half2(acc.x * r, acc.y * r);
   v.y = pack_half2(acc.z * r, acc.w * r);
   *reinterpret_cast<uint2*>(o) = v;
@@ -333,6 +334,7 @@ __device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int 
 
 }  // namespace
 
+template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
     partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const PartialParams p) {
@@ -354,6 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
   const int nseg = p.batch * p.num_kv_heads;
+  // per-tensor scales: host values, or device scalars read when the kernel runs
+  const float k_scale = p.k_scale_ptr ? __ldg(p.k_scale_ptr) : p.k_scale;
+  const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
+  const float scale_log2 = static_cast<float>(p.qk_scale_base * static_cast<double>(k_scale));
 
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -472,8 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&full_bar[slot]);
       } else {
         mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
-        tma_load_2d(st, &tm_k, &full_bar[slot], 0, y, policy);
-        tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, y, policy);
+        if (p.kv_layout == XQA_LAYOUT_HND) {
+          tma_load_2d(st, &tm_k, &full_bar[slot], 0, y, policy);
+          tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, y, policy);
+        } else {  // NHD: box (128 dims, 1 kv head, 16 tokens) at (0, kvh, page*16)
+          const int kvh = sg - (sg / p.num_kv_heads) * p.num_kv_heads;
+          tma_load_3d(st, &tm_k, &full_bar[slot], 0, kvh, y, policy);
+          tma_load_3d(st + kPageBytes, &tm_v, &full_bar[slot], 0, kvh, y, policy);
+        }
       }
     }
     __syncwarp();
@@ -521,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mwhole) {
         __half* o = p.out +
                     ((size_t)mb_b * p.num_q_heads + (size_t)mb_kvh * p.group + h) * kHeadDim + dq;
-        const float r = p.v_scale / L;
+        const float r = v_scale / L;
         uint2 v;
         if (any_poison) {
           const float nan = __int_as_float(0x7fc00000);
@@ -603,18 +615,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nv1 = min(kBlockSize, ctx - (j0 + kWarps) * kBlockSize);
       if (pair && !bad0 && !bad1) {
         const int nv[2] = {nv0, nv1};
-        process_pages<2>(st, regs, qf, nv, p.scale_log2, g, c);
+        process_pages<kFmt, 2>(st, regs, qf, nv, scale_log2, g, c);
       } else {
         if (bad0 || bad1) poisoned = 1;
         if (!bad0) {
           const PageRegs one[1] = {regs[0]};
           const int nv[1] = {nv0};
-          process_pages<1>(st, one, qf, nv, p.scale_log2, g, c);
+          process_pages<kFmt, 1>(st, one, qf, nv, scale_log2, g, c);
         }
         if (pair && !bad1) {
           const PageRegs one[1] = {regs[1]};
           const int nv[1] = {nv1};
-          process_pages<1>(st, one, qf, nv, p.scale_log2, g, c);
+          process_pages<kFmt, 1>(st, one, qf, nv, scale_log2, g, c);
         }
       }
     }
@@ -688,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < npend; ++i) {
       if (!pend_last[i]) continue;
       const int s = pend_seg[i];
-      merge_pieces(p, s, segs[s], segs[s + 1], total, n, tid >> 5, (tid & 31) * 4);
+      merge_pieces(p, s, segs[s], segs[s + 1], total, n, tid >> 5, (tid & 31) * 4, v_scale);
     }
   }
 
@@ -723,12 +735,17 @@ cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, partial_kernel, tm_k, tm_v, p);
+  if (p.kv_dtype == XQA_KV_E4M3)
+    return cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3>, tm_k, tm_v, p);
+  return cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2>, tm_k, tm_v, p);
 }
 
 cudaError_t set_partial_attributes() {
-  return cudaFuncSetAttribute(partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kPartialSmem);
+  cudaError_t e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPartialSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPartialSmem);
 }
 
 }  // namespace xqa

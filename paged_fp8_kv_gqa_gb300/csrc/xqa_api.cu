@@ -28,7 +28,7 @@ std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
 struct Resolved {
   int batch, hq, hkv, group, mbs, nb;
-  int nseg, n_max, min_pages, merge_mode;
+  int nseg, n_max, min_pages, merge_mode, kv_dtype, kv_layout;
   float sm_scale;
   xqa::WsLayout ws;
 };
@@ -45,6 +45,8 @@ xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
   if (s->max_blocks_per_seq < 1 || s->num_blocks < 1) return XQA_ERR_SHAPE;
   if (s->max_ctas < 0 || s->min_pages_per_cta < 0) return XQA_ERR_SHAPE;
   if (s->merge_mode != 0 && s->merge_mode != 1) return XQA_ERR_SHAPE;
+  if (s->kv_dtype != XQA_KV_E5M2 && s->kv_dtype != XQA_KV_E4M3) return XQA_ERR_SHAPE;
+  if (s->kv_layout != XQA_LAYOUT_HND && s->kv_layout != XQA_LAYOUT_NHD) return XQA_ERR_SHAPE;
   // int32 index arithmetic on the device: pool rows, total pages, segments
   const long long pool_rows = (long long)s->num_blocks * s->num_kv_heads * kBlockSize;
   const long long max_pages = (long long)s->batch * s->num_kv_heads * s->max_blocks_per_seq;
@@ -60,6 +62,8 @@ xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
   r->sm_scale = s->sm_scale > 0.f ? s->sm_scale : (float)(1.0 / sqrt((double)kHeadDim));
   r->min_pages = s->min_pages_per_cta > 0 ? s->min_pages_per_cta : xqa::kDefaultMinPagesPerCta;
   r->merge_mode = s->merge_mode;
+  r->kv_dtype = s->kv_dtype;
+  r->kv_layout = s->kv_layout;
   if (s->max_ctas > 0) {
     r->n_max = s->max_ctas;
   } else {
@@ -103,17 +107,30 @@ xqa_status_t ensure_device_setup() {
   return XQA_OK;
 }
 
-// 2-D view of a [NB, Hkv, BS, D] byte pool: x = D (128 B rows), y = NB*Hkv*BS;
-// box = one (page, kv head) slice of BS x D bytes, 128-byte swizzle.
+// HND pool [NB, Hkv, BS, D]: 2-D view x = D (128 B rows), y = NB*Hkv*BS; box =
+// one (page, kv head) slice of BS x D bytes.
+// NHD pool [NB, BS, Hkv, D]: 3-D view x = D, y = Hkv, z = NB*BS; box = (D, 1, BS),
+// the same 16 rows of 128 B in shared memory. Both with the 128-byte swizzle.
 xqa_status_t encode_pool_map(CUtensorMap* map, const uint8_t* pool, const Resolved& r) {
-  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)r.nb * r.hkv * kBlockSize};
-  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
-  cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)kBlockSize};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult res = g_encode.load(std::memory_order_acquire)(
-      map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(pool), dims, strides, box,
-      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult res;
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (r.kv_layout == XQA_LAYOUT_HND) {
+    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)r.nb * r.hkv * kBlockSize};
+    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+    cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)kBlockSize};
+    res = g_encode.load(std::memory_order_acquire)(
+        map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(pool), dims, strides, box,
+        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)r.hkv, (cuuint64_t)r.nb * kBlockSize};
+    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)r.hkv * kHeadDim};
+    cuuint32_t box[3] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kBlockSize};
+    res = g_encode.load(std::memory_order_acquire)(
+        map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(pool), dims, strides, box,
+        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return res == CUDA_SUCCESS ? XQA_OK : XQA_ERR_LAUNCH;
 }
 
@@ -144,11 +161,15 @@ xqa_status_t xqa_plan(const int32_t* context_lens, const xqa_shape_t* shape, voi
   return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
 }
 
-xqa_status_t xqa_attend_partial(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
-                                const int32_t* block_tables, const int32_t* context_lens,
-                                float k_scale, float v_scale, void* out,
-                                const xqa_shape_t* shape, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+xqa_status_t attend_partial_impl(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                 const int32_t* block_tables, const int32_t* context_lens,
+                                 float k_scale, float v_scale, const float* k_scale_ptr,
+                                 const float* v_scale_ptr, void* out, const xqa_shape_t* shape,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return XQA_ERR_NULL;
   Resolved r;
   xqa_status_t st = resolve(shape, &r);
@@ -180,15 +201,20 @@ xqa_status_t xqa_attend_partial(const void* q, const uint8_t* k_cache, const uin
   p.group = r.group;
   p.max_blocks_per_seq = r.mbs;
   p.num_blocks = r.nb;
-  p.scale_log2 = (float)((double)r.sm_scale * (double)k_scale * 1.4426950408889634);
+  p.kv_dtype = r.kv_dtype;
+  p.kv_layout = r.kv_layout;
+  p.qk_scale_base = (double)r.sm_scale * 1.4426950408889634;  // sm_scale * log2(e)
+  p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.k_scale_ptr = k_scale_ptr;
+  p.v_scale_ptr = v_scale_ptr;
   cudaError_t e = xqa::launch_partial(tm_k, tm_v, p, r.n_max, (cudaStream_t)stream);
   return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
 }
 
-xqa_status_t xqa_combine(const int32_t* context_lens, float v_scale, void* out,
-                         const xqa_shape_t* shape, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+xqa_status_t combine_impl(const int32_t* context_lens, float v_scale, const float* v_scale_ptr,
+                          void* out, const xqa_shape_t* shape, void* workspace,
+                          size_t workspace_bytes, void* stream) {
   if (!context_lens || !out) return XQA_ERR_NULL;
   Resolved r;
   xqa_status_t st = resolve(shape, &r);
@@ -207,8 +233,29 @@ xqa_status_t xqa_combine(const int32_t* context_lens, float v_scale, void* out,
   p.num_kv_heads = r.hkv;
   p.group = r.group;
   p.v_scale = v_scale;
+  p.v_scale_ptr = v_scale_ptr;
   cudaError_t e = xqa::launch_combine(p, r.nseg, (cudaStream_t)stream);
   return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+xqa_status_t xqa_attend_partial(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float k_scale, float v_scale, void* out,
+                                const xqa_shape_t* shape, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return attend_partial_impl(q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale,
+                             nullptr, nullptr, out, shape, workspace, workspace_bytes, stream);
+}
+
+xqa_status_t xqa_combine(const int32_t* context_lens, float v_scale, void* out,
+                         const xqa_shape_t* shape, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return combine_impl(context_lens, v_scale, nullptr, out, shape, workspace, workspace_bytes,
+                      stream);
 }
 
 xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
@@ -231,11 +278,45 @@ xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_
   return xqa_combine(context_lens, v_scale, out, shape, workspace, workspace_bytes, stream);
 }
 
+xqa_status_t xqa_decode_device_scales(const void* q, const uint8_t* k_cache,
+                                      const uint8_t* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, const float* k_scale,
+                                      const float* v_scale, void* out, const xqa_shape_t* shape,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !k_scale ||
+      !v_scale)
+    return XQA_ERR_NULL;
+  Resolved r;
+  xqa_status_t st = resolve(shape, &r);
+  if (st != XQA_OK) return st;
+  if ((st = check_workspace(r, workspace, workspace_bytes)) != XQA_OK) return st;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return XQA_ERR_ALIGN;
+  if ((st = ensure_device_setup()) != XQA_OK) return st;
+  if ((st = xqa_plan(context_lens, shape, workspace, workspace_bytes, stream)) != XQA_OK)
+    return st;
+  if ((st = attend_partial_impl(q, k_cache, v_cache, block_tables, context_lens, 0.f, 0.f,
+                                k_scale, v_scale, out, shape, workspace, workspace_bytes,
+                                stream)) != XQA_OK)
+    return st;
+  return combine_impl(context_lens, 0.f, v_scale, out, shape, workspace, workspace_bytes, stream);
+}
+
 xqa_status_t xqa_dequant_e5m2(const uint8_t* in, size_t n, float scale, uint16_t* out_fp16_bits,
                               float* out_f32, void* stream) {
   if (n == 0) return XQA_OK;
   if (!in || !out_fp16_bits) return XQA_ERR_NULL;
-  cudaError_t e = xqa::launch_dequant(in, n, scale, out_fp16_bits, out_f32, (cudaStream_t)stream);
+  cudaError_t e = xqa::launch_dequant(XQA_KV_E5M2, in, n, scale, out_fp16_bits, out_f32,
+                                      (cudaStream_t)stream);
+  return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
+}
+
+xqa_status_t xqa_dequant_e4m3(const uint8_t* in, size_t n, float scale, uint16_t* out_fp16_bits,
+                              float* out_f32, void* stream) {
+  if (n == 0) return XQA_OK;
+  if (!in || !out_fp16_bits) return XQA_ERR_NULL;
+  cudaError_t e = xqa::launch_dequant(XQA_KV_E4M3, in, n, scale, out_fp16_bits, out_f32,
+                                      (cudaStream_t)stream);
   return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
 }
 

@@ -150,6 +150,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 3-D tiled TMA load (NHD caches: x = dims, y = kv head, z = token row).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z),
+      "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -240,6 +251,50 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {
                : "memory");
   return old;
 }
+
+// ---------------------------------------------------------------------------
+// exact E4M3 -> fp16: every E4M3 value (and NaN) is an fp16 value; the
+// hardware conversion of a pair of codes is exact.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(pair16)));
+  return d;
+}
+
+// Per-format conversions in the two shapes the attention kernel needs:
+//   k_lo / k_hi: the two codes at bytes {0,1} / {2,3} of a word -> half2;
+//   v_pairs:     same-position codes of two words x, y -> half2
+//                {x0,y0}, {x1,y1}, {x2,y2}, {x3,y3}.
+template <int kFmt>
+struct KvConv;
+
+template <>
+struct KvConv<XQA_KV_E5M2> {
+  __device__ __forceinline__ static uint32_t k_lo(uint32_t w) { return e5m2x2_lo(w); }
+  __device__ __forceinline__ static uint32_t k_hi(uint32_t w) { return e5m2x2_hi(w); }
+  __device__ __forceinline__ static void v_pairs(uint32_t x, uint32_t y, uint32_t (&o)[4]) {
+    const uint32_t i01 = interleave01(x, y), i23 = interleave23(x, y);
+    o[0] = pair_even(i01);
+    o[1] = pair_odd(i01);
+    o[2] = pair_even(i23);
+    o[3] = pair_odd(i23);
+  }
+};
+
+template <>
+struct KvConv<XQA_KV_E4M3> {
+  __device__ __forceinline__ static uint32_t k_lo(uint32_t w) { return e4m3x2_to_f16x2(w & 0xffffu); }
+  __device__ __forceinline__ static uint32_t k_hi(uint32_t w) { return e4m3x2_to_f16x2(w >> 16); }
+  __device__ __forceinline__ static void v_pairs(uint32_t x, uint32_t y, uint32_t (&o)[4]) {
+    const uint32_t a = prmt(x, y, 0x5140u);  // {x0, y0, x1, y1}
+    const uint32_t b = prmt(x, y, 0x7362u);  // {x2, y2, x3, y3}
+    o[0] = e4m3x2_to_f16x2(a & 0xffffu);
+    o[1] = e4m3x2_to_f16x2(a >> 16);
+    o[2] = e4m3x2_to_f16x2(b & 0xffffu);
+    o[3] = e4m3x2_to_f16x2(b >> 16);
+  }
+};
 
 __device__ __forceinline__ void record_status(int32_t* status, int code) {
   atomicCAS(status, 0, code);

@@ -20,8 +20,11 @@ struct PartialParams {
   int batch, num_q_heads, num_kv_heads, group, max_blocks_per_seq, num_blocks;
   int n_max, min_pages;      // split rule inputs (same values the planner got)
   int fused_merge;           // 1: the last CTA of a split segment merges it
-  float scale_log2;  // sm_scale * k_scale * log2(e)
-  float v_scale;
+  int kv_dtype, kv_layout;   // XQA_KV_* code format, XQA_LAYOUT_* cache layout
+  double qk_scale_base;      // sm_scale * log2(e); the logit scale is this * k_scale
+  float k_scale, v_scale;    // per-tensor scales (used when the pointers are null)
+  const float* k_scale_ptr;  // optional device scalars, read when the kernel runs
+  const float* v_scale_ptr;
 };
 
 struct CombineParams {
@@ -32,6 +35,7 @@ struct CombineParams {
   const float* partials;
   int num_q_heads, num_kv_heads, group;
   float v_scale;
+  const float* v_scale_ptr;  // optional device scalar (overrides v_scale)
 };
 
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int num_kv_heads,
@@ -40,7 +44,7 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int num_kv_heads
 cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const PartialParams& p, int n_max, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int num_segments, cudaStream_t stream);
-cudaError_t launch_dequant(const uint8_t* in, size_t n, float scale, uint16_t* out16,
-                           float* out32, cudaStream_t stream);
+cudaError_t launch_dequant(int kv_dtype, const uint8_t* in, size_t n, float scale,
+                           uint16_t* out16, float* out32, cudaStream_t stream);
 
 }  // namespace xqa

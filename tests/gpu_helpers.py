@@ -28,7 +28,8 @@ def oracle_out(name: str) -> np.ndarray:
 
 def oracle_of(w: wl.Workload, sm_scale=None) -> np.ndarray:
     return attention.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables,
-                                            w.context_lens, w.k_scale, w.v_scale, sm_scale)
+                                            w.context_lens, w.k_scale, w.v_scale, sm_scale,
+                                            kv_dtype=w.kv_dtype, kv_layout=w.kv_layout)
 
 
 def to_dev(a: np.ndarray) -> torch.Tensor:
@@ -47,7 +48,7 @@ class Dev:
         self.bt = to_dev(w.block_tables)
         self.lens = to_dev(w.context_lens)
         self.shape = xqa.make_shape(self.q, self.k, self.bt, sm_scale, max_ctas, min_pages,
-                                    merge_mode)
+                                    merge_mode, kv_dtype=w.kv_dtype, kv_layout=w.kv_layout)
         self.out = torch.full_like(self.q, float("nan"))
         self.ws = xqa.alloc_workspace(self.shape)
 
