@@ -240,7 +240,9 @@ def run_gpu(args, world, rank, local, dist):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = workloads.make_workload(args.workload)
+    w = workloads.make_workload(args.workload, kv_dtype=args.kv_dtype)
+    if args.kv_layout == "nhd":
+        w = workloads.to_nhd(w)
     kv_bytes = w.kv_bytes
 
     def up(a):
@@ -252,7 +254,8 @@ def run_gpu(args, world, rank, local, dist):
     pools.append((k0, v0))
     for _ in range(args.pools - 1):
         pools.append((k0.clone(), v0.clone()))
-    shape = xqa.make_shape(q, k0, bt, merge_mode=args.merge_mode)
+    shape = xqa.make_shape(q, k0, bt, merge_mode=args.merge_mode, kv_dtype=args.kv_dtype,
+                           kv_layout=args.kv_layout)
     ws = xqa.alloc_workspace(shape, dev)
     out = torch.empty_like(q)
     stream = torch.cuda.Stream(device=dev)
@@ -375,7 +378,7 @@ def run_gpu(args, world, rank, local, dist):
                 for d, h in ((dq, hq), (dk, hk), (dv, hv), (dbt, hbt), (dl, hl)):
                     d.copy_(h, non_blocking=True)
                 xqa.xqa_decode(dq, dk, dv, dbt, dl, w.k_scale, w.v_scale, out=dout, workspace=ws,
-                               shape=shape, stream=stream)
+                               shape=shape, stream=stream)  # shape carries format and layout
                 hout.copy_(dout, non_blocking=True)
             stream.synchronize()
 
@@ -411,7 +414,7 @@ def run_gpu(args, world, rank, local, dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 mma / f32 acc (e5m2 kv)",
+        "dtype": f"f16 mma / f32 acc ({args.kv_dtype} kv)",
         "data": "synthetic",
         "config": {
             "workload": args.workload,
@@ -423,6 +426,8 @@ def run_gpu(args, world, rank, local, dist):
                   f"{2 * w.k_cache.nbytes / 1e6:.0f} MB",
             "timing": f"CUDA graph replays of {C} steps on one stream, CUDA events",
             "merge_mode": shape.merge_mode,
+            "kv_dtype": args.kv_dtype,
+            "kv_layout": args.kv_layout,
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "pct_of_nominal_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
@@ -540,6 +545,8 @@ def main(argv=None):
     ap.add_argument("--graph-steps", type=int, default=50)
     ap.add_argument("--event-every", type=int, default=10,
                     help="bracket every n-th step of the timed graph with CUDA events")
+    ap.add_argument("--kv-dtype", choices=("e5m2", "e4m3"), default="e5m2")
+    ap.add_argument("--kv-layout", choices=("hnd", "nhd"), default="hnd")
     ap.add_argument("--merge-mode", type=int, choices=(0, 1), default=0,
                     help="0: split segments merged inside the partial kernel; 1: combine kernel")
     ap.add_argument("--warm-seconds", type=float, default=1.0)
