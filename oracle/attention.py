@@ -132,3 +132,35 @@ def paged_decode_attention_rows(
         p = np.exp(s)
         res[i] = (p / p.sum()) @ v
     return res
+
+
+def paged_decode_attention_multi(
+    q: np.ndarray,
+    k_cache: np.ndarray,
+    v_cache: np.ndarray,
+    block_tables: np.ndarray,
+    context_lens: np.ndarray,
+    k_scale: float,
+    v_scale: float,
+    sm_scale: float | None = None,
+    kv_dtype: str = "e5m2",
+    kv_layout: str = "hnd",
+) -> np.ndarray:
+    """Decode of T new tokens per sequence: float64 [B, T, Hq, D].
+
+    ``q`` is [B, T, Hq, D]; ``context_lens[b]`` counts the T new tokens, whose
+    keys and values are already in the cache. New token i sits at position
+    ``ctx_b - T + i`` and attends causally to tokens ``0 .. ctx_b - T + i``
+    (none if that is negative: a zero row). Reading: the pages name multi-token
+    (MTP) decode only as a variant their target excluded ("no MTP", page
+    "[Kernel][SM70] Pipeline batched E5M2 XQA decode", section "Purpose").
+    Each new token is therefore a single-token decode over its causal prefix.
+    """
+    batch, t_new = q.shape[0], q.shape[1]
+    out = np.zeros(q.shape, dtype=np.float64)
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    for i in range(t_new):
+        visible = np.maximum(ctx - t_new + i + 1, 0).astype(np.int32)
+        out[:, i] = paged_decode_attention(q[:, i], k_cache, v_cache, block_tables, visible,
+                                           k_scale, v_scale, sm_scale, kv_dtype, kv_layout)
+    return out
