@@ -62,7 +62,7 @@ typedef enum xqa_status {
 #define XQA_LAYOUT_NHD 1 /* [NB, BS, Hkv, D]: token-major pages */
 
 /* Problem dimensions. head_dim must be 128 and block_size 16; Hq must be a
- * multiple of Hkv with G = Hq / Hkv <= 8. */
+ * multiple of Hkv with G = Hq / Hkv <= 8, and G * q_len <= 16. */
 typedef struct xqa_shape {
   int32_t batch;              /* B: sequences (one query token each), >= 1 */
   int32_t num_q_heads;        /* Hq */
@@ -80,6 +80,12 @@ typedef struct xqa_shape {
                                  combine kernel (xqa_combine) */
   int32_t kv_dtype;           /* XQA_KV_E5M2 (0, default) or XQA_KV_E4M3 */
   int32_t kv_layout;          /* XQA_LAYOUT_HND (0, default) or XQA_LAYOUT_NHD */
+  int32_t q_len;              /* T: new tokens per sequence; 0 or 1 = single-token
+                                 decode. With T > 1, q and out are [B, T, Hq, D],
+                                 context_lens count the T new tokens (their K/V
+                                 already in the cache) and new token i attends
+                                 causally to tokens 0 .. ctx_b - T + i (none if
+                                 negative: a zero row) */
 } xqa_shape_t;
 
 /* Bytes of device workspace xqa_decode needs for `shape` on the current
@@ -88,7 +94,8 @@ xqa_status_t xqa_workspace_size(const xqa_shape_t* shape, size_t* bytes);
 
 /* One decode step of paged GQA attention.
  *
- *   q             device, fp16 [B, Hq, D], contiguous, 16-byte aligned
+ *   q             device, fp16 [B, Hq, D] ([B, T, Hq, D] with q_len T > 1),
+ *                 contiguous, 16-byte aligned
  *   k_cache       device, FP8 codes (shape->kv_dtype) in the shape->kv_layout
  *                 layout: [NB, Hkv, BS, D] (HND: one (page, kv head) slice is
  *                 BS*D = 2048 contiguous bytes) or [NB, BS, Hkv, D] (NHD),
@@ -100,7 +107,7 @@ xqa_status_t xqa_workspace_size(const xqa_shape_t* shape, size_t* bytes);
  *   context_lens  device, int32 [B]; 0 <= ctx_b <= MBS*BS (0 gives a zero row)
  *   k_scale       per-tensor K scale (the key value is k_scale * FP8(code))
  *   v_scale       per-tensor V scale
- *   out           device, fp16 [B, Hq, D], contiguous, 16-byte aligned
+ *   out           device, fp16, same shape as q, contiguous, 16-byte aligned
  *   workspace     device, >= xqa_workspace_size bytes, 256-byte aligned; holds
  *                 the plan, the split partials and the status word; contents
  *                 need no initialisation and are overwritten every call
@@ -190,7 +197,7 @@ xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int3
  *
  *   - Shapes whose xqa_workspace_size exceeds XQA_STATIC_WORKSPACE_BYTES are
  *     rejected with XQA_ERR_WORKSPACE before anything is enqueued (for 152
- *     SMs: B * Hkv up to about 1800 segments).
+ *     SMs: B * Hkv up to about 850 segments).
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (that device must be current) and caches it; make
  *     that first call before any stream capture.

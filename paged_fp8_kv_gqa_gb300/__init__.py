@@ -68,6 +68,7 @@ class XqaShape(ctypes.Structure):
         ("merge_mode", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32),
         ("kv_layout", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
     ]
 
 
@@ -145,9 +146,13 @@ def _cuda(t: torch.Tensor, dtype, name: str) -> int:
 def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
                sm_scale: float = 0.0, max_ctas: int = 0, min_pages_per_cta: int = 0,
                merge_mode: int = 0, kv_dtype: str = "e5m2", kv_layout: str = "hnd") -> XqaShape:
-    """Shape descriptor from q [B, Hq, D], block_tables [B, MBS] and k_cache
-    [NB, Hkv, BS, D] (kv_layout "hnd") or [NB, BS, Hkv, D] ("nhd")."""
-    b, hq, d = q.shape
+    """Shape descriptor from q [B, Hq, D] (or [B, T, Hq, D] for T new tokens per
+    sequence), block_tables [B, MBS] and k_cache [NB, Hkv, BS, D] (kv_layout
+    "hnd") or [NB, BS, Hkv, D] ("nhd")."""
+    if q.dim() == 4:
+        b, t_new, hq, d = q.shape
+    else:
+        (b, hq, d), t_new = q.shape, 1
     if kv_layout == "hnd":
         nb, hkv, bs, d2 = k_cache.shape
     else:
@@ -156,7 +161,7 @@ def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tenso
         raise ValueError("inconsistent q / k_cache / block_tables shapes")
     return XqaShape(int(b), int(hq), int(hkv), int(d), int(bs), int(block_tables.shape[1]),
                     int(nb), float(sm_scale), int(max_ctas), int(min_pages_per_cta),
-                    int(merge_mode), KV_DTYPES[kv_dtype], KV_LAYOUTS[kv_layout])
+                    int(merge_mode), KV_DTYPES[kv_dtype], KV_LAYOUTS[kv_layout], int(t_new))
 
 
 def xqa_workspace_size(shape: XqaShape) -> int:

@@ -1,6 +1,7 @@
 // combine.cu — log-sum-exp merge of the split-KV partial results.
 //
-// One CTA per (sequence, kv head) segment. Segments processed whole by one
+// One CTA per (sequence, kv head) segment; a thread handles one column (new
+// token x head) and 4 dims at a time. Segments processed whole by one
 // partial CTA were already written by it; this kernel writes zero rows for
 // empty segments (context length 0), NaN rows for bad segments and, for a
 // segment split over CTAs i_lo..i_hi, merges their pieces (slot i + s):
@@ -23,51 +24,58 @@ __device__ __forceinline__ void store_half4(__half* dst, float a, float b, float
   *reinterpret_cast<uint2*>(dst) = v;
 }
 
+// Row of column col (new token i = col / G, head h = col % G) of segment s.
+__device__ __forceinline__ size_t combine_row(const CombineParams& p, int s, int col) {
+  const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+  const int i = col / p.group, h = col - i * p.group;
+  return ((size_t)b * p.q_len + i) * p.num_q_heads + (size_t)kvh * p.group + h;
+}
+
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
   const int s = blockIdx.x;
-  const int h = threadIdx.x >> 5;
   const int dq = (threadIdx.x & 31) * 4;
-  if (h >= p.group) return;
+  const int ncols = p.group * p.q_len;
   const int n = p.header[1];
   const long long total = p.header[2];
   const int sb = p.seg_start[s], se = p.seg_start[s + 1];
   const bool bad = p.seg_bad[s] != 0;
-  const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
-  __half* o = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim + dq;
-  if (sb == se) {
-    const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
-    store_half4(o, v, v, v, v);
-    return;
-  }
-  const int ilo = (int)(((long long)(sb + 1) * n - 1) / total);
-  const int ihi = (int)(((long long)se * n - 1) / total);
-  if (ilo == ihi) return;  // written whole by its partial CTA
-  if (bad) {
-    const float v = __int_as_float(0x7fc00000);
-    store_half4(o, v, v, v, v);
-    return;
-  }
-  float M = -INFINITY;
-  for (int i = ilo; i <= ihi; ++i) {
-    const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
-    M = fmaxf(M, slot[kMaxGroup * kHeadDim + h]);
-  }
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = ilo; i <= ihi; ++i) {
-    const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
-    const float mi = slot[kMaxGroup * kHeadDim + h];
-    const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
-    L += w * slot[kMaxGroup * kHeadDim + kMaxGroup + h];
-    const float4 v = *reinterpret_cast<const float4*>(slot + h * kHeadDim + dq);
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
-  }
   const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
-  const float r = v_scale / L;
-  store_half4(o, acc.x * r, acc.y * r, acc.z * r, acc.w * r);
+  for (int col = threadIdx.x >> 5; col < ncols; col += kCombineThreads / 32) {
+    __half* o = p.out + combine_row(p, s, col) * kHeadDim + dq;
+    if (sb == se) {
+      const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
+      store_half4(o, v, v, v, v);
+      continue;
+    }
+    const int ilo = (int)(((long long)(sb + 1) * n - 1) / total);
+    const int ihi = (int)(((long long)se * n - 1) / total);
+    if (ilo == ihi) continue;  // written whole by its partial CTA
+    if (bad) {
+      const float v = __int_as_float(0x7fc00000);
+      store_half4(o, v, v, v, v);
+      continue;
+    }
+    float M = -INFINITY;
+    for (int i = ilo; i <= ihi; ++i) {
+      const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
+      M = fmaxf(M, slot[kSlotM + col]);
+    }
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = ilo; i <= ihi; ++i) {
+      const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
+      const float mi = slot[kSlotM + col];
+      const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
+      L += w * slot[kSlotL + col];
+      const float4 v = *reinterpret_cast<const float4*>(slot + col * kHeadDim + dq);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    const float r = (L > 0.f) ? v_scale / L : 0.f;  // a new token with no visible token: 0
+    store_half4(o, acc.x * r, acc.y * r, acc.z * r, acc.w * r);
+  }
 }
 
 cudaError_t launch_combine(const CombineParams& p, int num_segments, cudaStream_t stream) {

@@ -10,26 +10,36 @@
 //
 // Every one of the 8 warps both loads and computes. Warp w owns the CTA-local
 // pages w, w+8, w+16, ... and the ring slots w, w+8, w+16, w+24 they map to
-// (slot = page % kStages). It keeps kLookahead of its pages in flight: after
-// computing page q it issues the two 2-D TMA loads (K and V slice, 2048 B each,
-// 128-byte swizzle) of its page q + kStages into the slot it just freed, so no
+// (slot = page % kStages). It keeps kLookahead of its pages in flight: once a
+// page is in registers it issues the two TMA loads (K and V slice, 2048 B each,
+// 128-byte swizzle) of its page q + kStages into the slot just freed, so no
 // empty-slot barrier is needed and TMA issue is spread over all warps. Block ids
 // are fetched 32 owned pages at a time, one batch ahead (bounds-checked).
 //
+// Columns: the MMA N dimension holds (new token i, q head h) pairs of one kv
+// head, column = i * G + h, 8 per tile; single-token decode has G columns and
+// one tile, multi-token decode up to 16 columns in two tiles (NT).
+//
 // Per 16-token page a warp
 //   - reads K and V with conflict-free 16-byte shared loads,
-//   - dequantises exactly (fp16 pattern = code << 8, a byte permutation),
-//   - S^T[16 tok x 8 heads] = K * Q^T with 8 m16n8k16 MMAs (fp32 accumulate),
-//   - runs the online softmax in the log2 domain (k_scale and sm_scale folded
-//     into one fp32 logit scale; the running max only moves when a logit
-//     exceeds it by more than 8, so most pages skip the rescale),
-//   - moves P^T to the B-operand layout with two movmatrix transposes,
-//   - O^T[128 x 8] += V^T * P^T with 8 MMAs plus one MMA against ones for the
-//     row sums l (so l sums exactly the fp16 P used for O).
-// At the end of every segment the 8 warps' (m, l, O) are merged in shared
-// memory; a segment owned whole by this CTA is normalised and written as fp16
-// (out = O * (v_scale / l)); otherwise the piece goes to partial slot i + s for
-// the combine kernel.
+//   - dequantises exactly (E5M2: fp16 pattern = code << 8, a byte permutation;
+//     E4M3: the hardware pair conversion),
+//   - S^T[16 tok x 8 cols] = K * Q^T with 8 m16n8k16 MMAs per tile (fp32 acc),
+//   - masks tokens past each column's causal limit (ctx - 1 for single-token
+//     decode), then runs the online softmax in the log2 domain (k_scale and
+//     sm_scale folded into one fp32 logit scale; the running max only moves
+//     when a logit exceeds it by more than 8, so most pages skip the rescale),
+//   - moves P^T to the B-operand layout with two movmatrix transposes per tile,
+//   - O^T[128 x 8] += V^T * P^T with 8 MMAs per tile (V converted once for all
+//     tiles) plus one MMA against ones for the row sums l (so l sums exactly
+//     the fp16 P used for O).
+// With one tile a warp takes its pages two at a time, interleaving two
+// independent dependency chains. At the end of a segment each warp hands its
+// (m, l, O) to a shared merge buffer and moves on; the buffered segments are
+// merged across warps when a buffer is reused and at the end of the range. A
+// segment owned whole by this CTA is normalised and written as fp16
+// (out = O * (v_scale / l)); a split piece goes to partial slot i + s, and the
+// CTA whose ticket completes the segment merges all its pieces.
 //
 // Contraction-index permutation: the MMA result does not depend on how the
 // contraction index is laid out, as long as both operands use the same layout.
@@ -54,19 +64,6 @@ __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
 
-__device__ __forceinline__ int consumer_bar_or(int pred) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.s32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, %2, p;\n\t"
-      "selp.s32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(pred), "n"(kThreads)
-      : "memory");
-  return r;
-}
-
 // Largest s in [lo, nseg) with seg_start[s] <= page, given seg_start[lo] <= page
 // < seg_start[nseg]. `seg_start` may point to shared or global memory.
 __device__ __forceinline__ int find_segment(const int32_t* seg_start, int lo, int nseg, int page) {
@@ -81,7 +78,7 @@ __device__ __forceinline__ int find_segment(const int32_t* seg_start, int lo, in
 
 // TMA coordinates of 32 consecutive owned pages of one warp, one per lane.
 struct PageBatch {
-  int y;    // row of the (page, kv head) slice in the [NB*Hkv*16, 128] view
+  int y;    // HND: row of the (page, kv head) slice; NHD: first token row of the page
   int bad;  // block id outside [0, NB)
   int seg;  // segment of the page
 };
@@ -98,49 +95,64 @@ __device__ __forceinline__ PageBatch load_batch(const PartialParams& p, const in
     const int j = pg - segs[s];
     const int id = __ldg(&p.block_tables[(size_t)b * p.max_blocks_per_seq + j]);
     r.bad = (id < 0 || id >= p.num_blocks) ? 1 : 0;
-    // HND: row of the (page, kv head) slice; NHD: first token row of the page
     r.y = r.bad ? 0 : (p.kv_layout == XQA_LAYOUT_HND ? (id * p.num_kv_heads + kvh) : id) * kBlockSize;
     r.seg = s;
   }
   return r;
 }
 
-// Q of segment s as B fragments: lane (g, c) holds head g, dims [32c, 32c+32).
-__device__ __forceinline__ void load_q(const PartialParams& p, int s, int g, int c,
-                                       uint32_t (&qf)[16]) {
+// Output / query row of column col (new token i = col / G, head h = col % G)
+// of segment s: ((b * T + i) * Hq + kvh * G + h).
+__device__ __forceinline__ size_t col_row(const PartialParams& p, int s, int col) {
   const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
-  if (g < p.group) {
-    const uint4* qp = reinterpret_cast<const uint4*>(
-        p.q + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + g) * kHeadDim + 32 * c);
+  const int i = col / p.group, h = col - i * p.group;
+  return ((size_t)b * p.q_len + i) * p.num_q_heads + (size_t)kvh * p.group + h;
+}
+
+// Q of segment s as B fragments: lane (g, c) holds column 8j + g of tile j,
+// dims [32c, 32c+32); columns past G * q_len are zero.
+template <int NT>
+__device__ __forceinline__ void load_q(const PartialParams& p, int s, int g, int c,
+                                       uint32_t (&qf)[NT][16]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = __ldg(qp + i);
-      qf[4 * i] = v.x;
-      qf[4 * i + 1] = v.y;
-      qf[4 * i + 2] = v.z;
-      qf[4 * i + 3] = v.w;
+  for (int j = 0; j < NT; ++j) {
+    const int col = 8 * j + g;
+    if (col < p.group * p.q_len) {
+      const uint4* qp = reinterpret_cast<const uint4*>(p.q + col_row(p, s, col) * kHeadDim + 32 * c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldg(qp + i);
+        qf[j][4 * i] = v.x;
+        qf[j][4 * i + 1] = v.y;
+        qf[j][4 * i + 2] = v.z;
+        qf[j][4 * i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) qf[j][i] = 0u;
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) qf[i] = 0u;
   }
 }
 
+template <int NT>
 struct WarpState {
-  float o[8][4];  // O^T tiles: [tile i][c-frag]; rows d = 16g + 2i (+1), cols heads 2c (+1)
-  float l[4];     // row sums per head (cols 2c, 2c+1), replicated over rows
-  float m0, m1;   // running max (log2 domain) of heads 2c and 2c+1
+  float o[NT][8][4];  // O^T tiles per column tile: rows d = 16g + 2i (+1), cols 2c (+1)
+  float l[NT][4];     // row sums per column (2c, 2c+1), replicated over rows
+  float m[NT][2];     // running max (log2 domain) of columns 2c and 2c+1
 };
 
-__device__ __forceinline__ void reset_state(WarpState& st) {
+template <int NT>
+__device__ __forceinline__ void reset_state(WarpState<NT>& st) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int j = 0; j < NT; ++j) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) st.o[i][k] = 0.f;
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-  for (int k = 0; k < 4; ++k) st.l[k] = 0.f;
-  st.m0 = -INFINITY;
-  st.m1 = -INFINITY;
+      for (int k = 0; k < 4; ++k) st.o[j][i][k] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st.l[j][k] = 0.f;
+    st.m[j][0] = st.m[j][1] = -INFINITY;
+  }
 }
 
 // One page's K and V bytes as this lane needs them (see the layout note above).
@@ -165,16 +177,27 @@ __device__ __forceinline__ PageRegs load_page(const uint8_t* ks, const uint8_t* 
   return r;
 }
 
-// NP (1 or 2) 16-token pages of one kv head: QK, one online-softmax update for
-// all NP pages, PV. With two pages the two independent QK and PV chains
-// interleave, which hides the fixed latencies of one page's chain behind the
-// other's.
-template <int kFmt, int NP>
-__device__ __forceinline__ void process_pages(WarpState& st, const PageRegs (&r)[NP],
-                                              const uint32_t (&qf)[16], const int (&nvalid)[NP],
+// Causal limits of one segment for this lane: token t is visible to column
+// 8j + 2c + e iff t <= lim[j][e] (ctx - T + i; ctx - 1 for single-token
+// decode). Padding columns never mask. min_lim is the smallest limit of a real
+// column: a page whose last token is at most min_lim needs no mask at all.
+template <int NT>
+struct SegLimits {
+  int lim[NT][2];
+  int min_lim;
+};
+
+// NP 16-token pages (NP = 2 only with one column tile) of one kv head: QK for
+// every column tile, one online-softmax update, PV for every tile. The V
+// fragments are converted once and shared by all tiles. With two pages the two
+// independent chains interleave and hide each other's fixed latencies.
+template <int kFmt, int NP, int NT>
+__device__ __forceinline__ void process_pages(WarpState<NT>& st, const PageRegs (&r)[NP],
+                                              const uint32_t (&qf)[NT][16], const int (&tok0)[NP],
+                                              const int (&nvalid)[NP], const SegLimits<NT>& sl,
                                               float scale_log2, int g, int c) {
-  // ---- S^T = K * Q^T : rows tokens (g, g+8), cols heads (2c, 2c+1) ----
-  float s[NP][4];
+  // ---- S^T = K * Q^T : rows tokens (g, g+8), cols 2c, 2c+1 of each tile ----
+  float s[NP][NT][4];
 #pragma unroll
   for (int pi = 0; pi < NP; ++pi) {
     const uint32_t kr0[8] = {r[pi].ka0.x, r[pi].ka0.y, r[pi].ka0.z, r[pi].ka0.w,
@@ -182,62 +205,88 @@ __device__ __forceinline__ void process_pages(WarpState& st, const PageRegs (&r)
     const uint32_t kr1[8] = {r[pi].kb0.x, r[pi].kb0.y, r[pi].kb0.z, r[pi].kb0.w,
                              r[pi].kb1.x, r[pi].kb1.y, r[pi].kb1.z, r[pi].kb1.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) s[pi][k] = 0.f;
+    for (int j = 0; j < NT; ++j)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      mma_16816(s[pi], KvConv<kFmt>::k_lo(kr0[j]), KvConv<kFmt>::k_lo(kr1[j]),
-                KvConv<kFmt>::k_hi(kr0[j]), KvConv<kFmt>::k_hi(kr1[j]), qf[2 * j],
-                qf[2 * j + 1]);
+      for (int k = 0; k < 4; ++k) s[pi][j][k] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t a0 = KvConv<kFmt>::k_lo(kr0[kk]), a1 = KvConv<kFmt>::k_lo(kr1[kk]);
+      const uint32_t a2 = KvConv<kFmt>::k_hi(kr0[kk]), a3 = KvConv<kFmt>::k_hi(kr1[kk]);
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+        mma_16816(s[pi][j], a0, a1, a2, a3, qf[j][2 * kk], qf[j][2 * kk + 1]);
     }
   }
 
   // ---- online softmax (log2 domain), one update for all NP pages ----
-  float t[NP][4];
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+  float t[NP][NT][4];
+  float mx[NT][2];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) mx[j][0] = mx[j][1] = -INFINITY;
 #pragma unroll
   for (int pi = 0; pi < NP; ++pi) {
+    const bool masked = tok0[pi] + kBlockSize - 1 > sl.min_lim;
+    const int r0 = tok0[pi] + g, r1 = tok0[pi] + g + 8;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) t[pi][k] = s[pi][k] * scale_log2;
-    if (nvalid[pi] < kBlockSize) {
-      if (g >= nvalid[pi]) t[pi][0] = t[pi][1] = -INFINITY;
-      if (g + 8 >= nvalid[pi]) t[pi][2] = t[pi][3] = -INFINITY;
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) t[pi][j][k] = s[pi][j][k] * scale_log2;
+      if (masked) {
+        if (r0 > sl.lim[j][0]) t[pi][j][0] = -INFINITY;
+        if (r0 > sl.lim[j][1]) t[pi][j][1] = -INFINITY;
+        if (r1 > sl.lim[j][0]) t[pi][j][2] = -INFINITY;
+        if (r1 > sl.lim[j][1]) t[pi][j][3] = -INFINITY;
+      }
+      mx[j][0] = fmaxf(mx[j][0], fmaxf(t[pi][j][0], t[pi][j][2]));
+      mx[j][1] = fmaxf(mx[j][1], fmaxf(t[pi][j][1], t[pi][j][3]));
     }
-    mx0 = fmaxf(mx0, fmaxf(t[pi][0], t[pi][2]));
-    mx1 = fmaxf(mx1, fmaxf(t[pi][1], t[pi][3]));
   }
-  const bool need = (mx0 > st.m0 + kRescaleThreshold) || (mx1 > st.m1 + kRescaleThreshold);
+  bool need = false;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+    need = need || (mx[j][0] > st.m[j][0] + kRescaleThreshold) ||
+           (mx[j][1] > st.m[j][1] + kRescaleThreshold);
   if (__any_sync(kFull, need)) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-    }
-    const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
-    const float a0 = ex2(st.m0 - n0), a1 = ex2(st.m1 - n1);
-    st.m0 = n0;
-    st.m1 = n1;
+    for (int j = 0; j < NT; ++j) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      st.o[i][0] *= a0;
-      st.o[i][2] *= a0;
-      st.o[i][1] *= a1;
-      st.o[i][3] *= a1;
+      for (int off = 4; off < 32; off <<= 1) {
+        mx[j][0] = fmaxf(mx[j][0], __shfl_xor_sync(kFull, mx[j][0], off));
+        mx[j][1] = fmaxf(mx[j][1], __shfl_xor_sync(kFull, mx[j][1], off));
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float nm = fmaxf(st.m[j][e], mx[j][e]);
+        // a column that has seen no visible token yet keeps max -inf and an
+        // all-zero state: its rescale factor is 1, not 2^(-inf - -inf)
+        const float a = (nm == -INFINITY) ? 1.f : ex2(st.m[j][e] - nm);
+        st.m[j][e] = nm;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          st.o[j][i][e] *= a;
+          st.o[j][i][e + 2] *= a;
+        }
+        st.l[j][e] *= a;
+        st.l[j][e + 2] *= a;
+      }
     }
-    st.l[0] *= a0;
-    st.l[2] *= a0;
-    st.l[1] *= a1;
-    st.l[3] *= a1;
   }
 
 #pragma unroll
   for (int pi = 0; pi < NP; ++pi) {
-    const float p0 = ex2(t[pi][0] - st.m0), p1 = ex2(t[pi][1] - st.m1);
-    const float p2 = ex2(t[pi][2] - st.m0), p3 = ex2(t[pi][3] - st.m1);
-    // P^T B-fragments: lane (g, c) gets P[tokens 2c, 2c+1 | 2c+8, 2c+9][head g]
-    const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));
+    // P^T B-fragments per tile: lane (g, c) gets P[tokens 2c, 2c+1 | 2c+8, 2c+9][col g]
+    uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const float m0 = st.m[j][0] == -INFINITY ? 0.f : st.m[j][0];
+      const float m1 = st.m[j][1] == -INFINITY ? 0.f : st.m[j][1];
+      const float p0 = ex2(t[pi][j][0] - m0), p1 = ex2(t[pi][j][1] - m1);
+      const float p2 = ex2(t[pi][j][2] - m0), p3 = ex2(t[pi][j][3] - m1);
+      pb0[j] = movmatrix_trans(pack_half2(p0, p1));
+      pb1[j] = movmatrix_trans(pack_half2(p2, p3));
+    }
 
-    // ---- O^T += V^T * P^T ----
+    // ---- O^T += V^T * P^T for every tile ----
     uint4 vx = r[pi].vx, vy = r[pi].vy, vz = r[pi].vz, vw = r[pi].vw;
     if (nvalid[pi] < kBlockSize) {  // zero V rows past the context (0 * NaN would poison O)
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -253,27 +302,35 @@ __device__ __forceinline__ void process_pages(WarpState& st, const PageRegs (&r)
       uint32_t xy[4], zw[4];  // {x_k, y_k}: tokens 2c, 2c+1 / 2c+8, 2c+9 at dim byte k
       KvConv<kFmt>::v_pairs(X[u], Y[u], xy);
       KvConv<kFmt>::v_pairs(Z[u], W[u], zw);
-      mma_16816(st.o[2 * u], xy[0], xy[1], zw[0], zw[1], pb0, pb1);
-      mma_16816(st.o[2 * u + 1], xy[2], xy[3], zw[2], zw[3], pb0, pb1);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        mma_16816(st.o[j][2 * u], xy[0], xy[1], zw[0], zw[1], pb0[j], pb1[j]);
+        mma_16816(st.o[j][2 * u + 1], xy[2], xy[3], zw[2], zw[3], pb0[j], pb1[j]);
+      }
     }
-    mma_16816(st.l, kOnesHalf2, kOnesHalf2, kOnesHalf2, kOnesHalf2, pb0, pb1);
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+      mma_16816(st.l[j], kOnesHalf2, kOnesHalf2, kOnesHalf2, kOnesHalf2, pb0[j], pb1[j]);
   }
 }
 
-// LSE merge of all pieces of split segment s into fp16 rows (thread: head h,
-// dims dq..dq+3). Pieces were written by other CTAs: read through L2.
-__device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int sb, int se,
-                                             int total, int n, int h, int dq, float v_scale) {
-  if (h >= p.group) return;
-  const int ilo = cta_of_page(sb, total, n), ihi = cta_of_page(se - 1, total, n);
-  const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
-  __half* o = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim + dq;
+__device__ __forceinline__ void store_half4(__half* o, float a, float b, float c, float d) {
   uint2 v;
+  v.x = pack_half2(a, b);
+  v.y = pack_half2(c, d);
+  *reinterpret_cast<uint2*>(o) = v;
+}
+
+// LSE merge of all pieces of split segment s into fp16 rows (thread: column
+// col, dims dq..dq+3). Pieces were written by other CTAs: read through L2.
+__device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int sb, int se,
+                                             int total, int n, int col, int dq, float v_scale) {
+  if (col >= p.group * p.q_len) return;
+  const int ilo = cta_of_page(sb, total, n), ihi = cta_of_page(se - 1, total, n);
+  __half* o = p.out + col_row(p, s, col) * kHeadDim + dq;
   if (__ldcg(&p.seg_bad[s]) != 0) {
     const float nan = __int_as_float(0x7fc00000);
-    v.x = pack_half2(nan, nan);
-    v.y = v.x;
-    *reinterpret_cast<uint2*>(o) = v;
+    store_half4(o, nan, nan, nan, nan);
     return;
   }
   float M = -INFINITY;
@@ -288,9 +345,9 @@ __device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int 
     for (int k = 0; k < kFew; ++k) {
       if (ilo + k <= ihi) {
         const float* slot = p.partials + (size_t)(ilo + k + s) * kSlotFloats;
-        mi[k] = __ldcg(slot + kMaxGroup * kHeadDim + h);
-        li[k] = __ldcg(slot + kMaxGroup * kHeadDim + kMaxGroup + h);
-        oi[k] = __ldcg(reinterpret_cast<const float4*>(slot + h * kHeadDim + dq));
+        mi[k] = __ldcg(slot + kSlotM + col);
+        li[k] = __ldcg(slot + kSlotL + col);
+        oi[k] = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
       }
     }
 #pragma unroll
@@ -307,37 +364,35 @@ __device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int 
         acc.w += w * oi[k].w;
       }
     }
-    const float r = v_scale / L;
-    v.x = pack_half2(acc.x * r, acc.y * r);
-    v.y = pack_half2(acc.z * r, acc.w * r);
-    *reinterpret_cast<uint2*>(o) = v;
-    return;
+  } else {
+    for (int i = ilo; i <= ihi; ++i)
+      M = fmaxf(M, __ldcg(p.partials + (size_t)(i + s) * kSlotFloats + kSlotM + col));
+    for (int i = ilo; i <= ihi; ++i) {
+      const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
+      const float mi = __ldcg(slot + kSlotM + col);
+      const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
+      L += w * __ldcg(slot + kSlotL + col);
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
+      acc.x += w * x.x;
+      acc.y += w * x.y;
+      acc.z += w * x.z;
+      acc.w += w * x.w;
+    }
   }
-  for (int i = ilo; i <= ihi; ++i)
-    M = fmaxf(M, __ldcg(p.partials + (size_t)(i + s) * kSlotFloats + kMaxGroup * kHeadDim + h));
-  for (int i = ilo; i <= ihi; ++i) {
-    const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
-    const float mi = __ldcg(slot + kMaxGroup * kHeadDim + h);
-    const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
-    L += w * __ldcg(slot + kMaxGroup * kHeadDim + kMaxGroup + h);
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(slot + h * kHeadDim + dq));
-    acc.x += w * x.x;
-    acc.y += w * x.y;
-    acc.z += w * x.z;
-    acc.w += w * x.w;
-  }
-  const float r = v_scale / L;
-  v.x = pack_half2(acc.x * r, acc.y * r);
-  v.y = pack_half2(acc.z * r, acc.w * r);
-  *reinterpret_cast<uint2*>(o) = v;
+  const float rr = (L > 0.f) ? v_scale / L : 0.f;  // a new token with no visible token: 0
+  store_half4(o, acc.x * rr, acc.y * rr, acc.z * rr, acc.w * rr);
 }
 
 }  // namespace
 
-template <int kFmt>
+template <int kFmt, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const PartialParams p) {
+  using Geom = PartialGeom<NT>;
+  constexpr int kCols = Geom::kCols;
+  constexpr int kBufs = Geom::kMergeBufs;
+  constexpr bool kPairs = NT == 1;  // two pages per warp iteration
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ int stage_bad[kStages];
@@ -351,11 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int npend;
   // the segment each merge buffer holds, whether this CTA owns it whole, and
   // each warp's "met a bad page" flag for it
-  __shared__ int buf_seg[kMergeBufs], buf_whole[kMergeBufs], buf_poison[kMergeBufs][kWarps];
+  __shared__ int buf_seg[kBufs], buf_whole[kBufs], buf_poison[kBufs][kWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
   const int nseg = p.batch * p.num_kv_heads;
+  const int ncols = p.group * p.q_len;
   // per-tensor scales: host values, or device scalars read when the kernel runs
   const float k_scale = p.k_scale_ptr ? __ldg(p.k_scale_ptr) : p.k_scale;
   const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
@@ -364,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* merge_bufs = reinterpret_cast<float*>(stages + kStages * kStageBytes);
-  int32_t* seg_cache = reinterpret_cast<int32_t*>(merge_bufs + kMergeBufs * kMergeBufFloats);
+  int32_t* seg_cache = reinterpret_cast<int32_t*>(merge_bufs + kBufs * Geom::kMergeBufFloats);
 
   // ---- the plan: computed here when the segment table fits in shared memory
   // (same integer rule as the planner kernel), else read from the planner ----
@@ -417,16 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
     for (int s = warp; s < nseg; s += kWarps) {
       if (segs[s] != segs[s + 1]) continue;
-      const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
-      const int ctx = __ldg(&p.context_lens[b]);
+      const int ctx = __ldg(&p.context_lens[s / p.num_kv_heads]);
       const bool bad = ctx < 0 || (long long)ctx > max_ctx;
       const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
       uint4 val;
       val.x = val.y = val.z = val.w = pack_half2(v, v);
-      for (int i = lane; i < p.group * (kHeadDim / 8); i += 32) {
-        const int h = i / (kHeadDim / 8), d8 = i - h * (kHeadDim / 8);
-        __half* o = p.out + ((size_t)b * p.num_q_heads + (size_t)kvh * p.group + h) * kHeadDim;
-        reinterpret_cast<uint4*>(o)[d8] = val;
+      for (int i = lane; i < ncols * (kHeadDim / 8); i += 32) {
+        const int col = i / (kHeadDim / 8), d8 = i - col * (kHeadDim / 8);
+        reinterpret_cast<uint4*>(p.out + col_row(p, s, col) * kHeadDim)[d8] = val;
       }
     }
   }
@@ -494,11 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = 0; i < kLookahead; ++i) issue_next();
 
   if (tid == 0) npend = 0;
-  WarpState st;
-  uint32_t qf[16], qf_next[16];
+  WarpState<NT> st;
+  uint32_t qf[NT][16], qf_next[NT][16];
   int q_next_seg = -1;
-  // Merge of one buffered segment by all threads (head h, dims dq..dq+3): the
-  // 8 warps' (m, l, O) combine in shared memory; a segment owned whole is
+  // Merge of one buffered segment by all threads (column col, dims dq..dq+3):
+  // the 8 warps' (m, l, O) combine in shared memory; a segment owned whole is
   // normalised and written as fp16, a split piece goes to partial slot cta + s.
   auto merge_buffer = [&](int mb) {
     const int ms = buf_seg[mb];
@@ -506,50 +560,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     int any_poison = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) any_poison |= buf_poison[mb][w];
-    const float* base = merge_bufs + mb * kMergeBufFloats;
-    const float* bm = base + kScratchFloats;
-    const float* bl = bm + kWarps * kMaxGroup;
-    const int h = tid >> 5;         // 0..7
+    const float* base = merge_bufs + mb * Geom::kMergeBufFloats;
+    const float* bm = base + Geom::kScratchFloats;
+    const float* bl = bm + kWarps * kCols;
     const int dq = (tid & 31) * 4;  // 0..124
-    float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, bm[w * kMaxGroup + h]);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int col = tid >> 5; col < kCols; col += kWarps) {
+      if (col >= ncols) break;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float mw = bm[w * kMaxGroup + h];
-      const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-      L += sc * bl[w * kMaxGroup + h];
-      const float4 v =
-          *reinterpret_cast<const float4*>(base + (w * kMaxGroup + h) * kScratchStride + dq);
-      acc.x += sc * v.x;
-      acc.y += sc * v.y;
-      acc.z += sc * v.z;
-      acc.w += sc * v.w;
-    }
-    const int mb_b = ms / p.num_kv_heads, mb_kvh = ms - mb_b * p.num_kv_heads;
-    if (h < p.group) {
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, bm[w * kCols + col]);
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = bm[w * kCols + col];
+        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        L += sc * bl[w * kCols + col];
+        const float4 v =
+            *reinterpret_cast<const float4*>(base + (w * kCols + col) * kScratchStride + dq);
+        acc.x += sc * v.x;
+        acc.y += sc * v.y;
+        acc.z += sc * v.z;
+        acc.w += sc * v.w;
+      }
       if (mwhole) {
-        __half* o = p.out +
-                    ((size_t)mb_b * p.num_q_heads + (size_t)mb_kvh * p.group + h) * kHeadDim + dq;
-        const float r = v_scale / L;
-        uint2 v;
+        __half* o = p.out + col_row(p, ms, col) * kHeadDim + dq;
         if (any_poison) {
           const float nan = __int_as_float(0x7fc00000);
-          v.x = pack_half2(nan, nan);
-          v.y = v.x;
+          store_half4(o, nan, nan, nan, nan);
         } else {
-          v.x = pack_half2(acc.x * r, acc.y * r);
-          v.y = pack_half2(acc.z * r, acc.w * r);
+          const float rr = (L > 0.f) ? v_scale / L : 0.f;
+          store_half4(o, acc.x * rr, acc.y * rr, acc.z * rr, acc.w * rr);
         }
-        *reinterpret_cast<uint2*>(o) = v;
       } else {
         float* slotp = p.partials + (size_t)(cta + ms) * kSlotFloats;
-        *reinterpret_cast<float4*>(slotp + h * kHeadDim + dq) = acc;
+        *reinterpret_cast<float4*>(slotp + col * kHeadDim + dq) = acc;
         if (dq == 0) {
-          slotp[kMaxGroup * kHeadDim + h] = M;
-          slotp[kMaxGroup * kHeadDim + kMaxGroup + h] = L;
+          slotp[kSlotM + col] = M;
+          slotp[kSlotL + col] = L;
         }
       }
     }
@@ -567,25 +616,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (segs[s + 1] <= cbeg + q0) ++s;
     const int sb = segs[s], se = segs[s + 1];
     const int qe = min(se, cend) - cbeg;
-    const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
+    const int b = s / p.num_kv_heads;
     const int ctx = __ldg(&p.context_lens[b]);
     const bool whole = (sb >= cbeg) && (se <= cend);
     if (q_next_seg == s) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) qf[i] = qf_next[i];
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qf[j][i] = qf_next[j][i];
     } else {
-      load_q(p, s, g, c, qf);
+      load_q<NT>(p, s, g, c, qf);
     }
     if (qe < npages) {  // prefetch Q of the next segment this CTA works on
       q_next_seg = find_segment(segs, s, nseg, cbeg + qe);
-      load_q(p, q_next_seg, g, c, qf_next);
+      load_q<NT>(p, q_next_seg, g, c, qf_next);
     }
-    reset_state(st);
+    SegLimits<NT> sl;
+    sl.min_lim = ctx - p.q_len;  // the first new token's last visible token
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = 8 * j + 2 * c + e;
+        sl.lim[j][e] = col < ncols ? ctx - p.q_len + col / p.group : 0x7fffffff;
+      }
+    reset_state<NT>(st);
     int poisoned = 0;
 
-    // this warp's pages of the segment, two at a time (q and q + kWarps)
-    for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe; q += 2 * kWarps) {
-      const bool pair = q + kWarps < qe;
+    // this warp's pages of the segment (q, and q + kWarps when pairing)
+    for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe;
+         q += (kPairs ? 2 : 1) * kWarps) {
+      const bool pair = kPairs && q + kWarps < qe;
       const int slot0 = q % kStages, slot1 = (q + kWarps) % kStages;
       bool ready = mbar_wait_bounded(&full_bar[slot0], (q / kStages) & 1, abort);
       if (pair) ready = ready && mbar_wait_bounded(&full_bar[slot1], ((q + kWarps) / kStages) & 1, abort);
@@ -610,53 +671,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_next();
         if (pair) issue_next();
       }
-      const int j0 = cbeg + q - sb;
-      const int nv0 = min(kBlockSize, ctx - j0 * kBlockSize);
-      const int nv1 = min(kBlockSize, ctx - (j0 + kWarps) * kBlockSize);
-      if (pair && !bad0 && !bad1) {
-        const int nv[2] = {nv0, nv1};
-        process_pages<kFmt, 2>(st, regs, qf, nv, scale_log2, g, c);
+      const int j0 = cbeg + q - sb;  // page index within the sequence
+      const int t0 = j0 * kBlockSize, t1 = (j0 + kWarps) * kBlockSize;
+      const int nv0 = min(kBlockSize, ctx - t0), nv1 = min(kBlockSize, ctx - t1);
+      if (kPairs && pair && !bad0 && !bad1) {
+        const int tk[2] = {t0, t1}, nv[2] = {nv0, nv1};
+        process_pages<kFmt, 2, NT>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
       } else {
         if (bad0 || bad1) poisoned = 1;
         if (!bad0) {
           const PageRegs one[1] = {regs[0]};
-          const int nv[1] = {nv0};
-          process_pages<kFmt, 1>(st, one, qf, nv, scale_log2, g, c);
+          const int tk[1] = {t0}, nv[1] = {nv0};
+          process_pages<kFmt, 1, NT>(st, one, qf, tk, nv, sl, scale_log2, g, c);
         }
         if (pair && !bad1) {
           const PageRegs one[1] = {regs[1]};
-          const int nv[1] = {nv1};
-          process_pages<kFmt, 1>(st, one, qf, nv, scale_log2, g, c);
+          const int tk[1] = {t1}, nv[1] = {nv1};
+          process_pages<kFmt, 1, NT>(st, one, qf, tk, nv, sl, scale_log2, g, c);
         }
       }
     }
 
-    // ---- hand this segment's per-warp state to a merge buffer; no CTA-wide
-    // barrier unless the buffer still holds the segment before the previous
-    // one (so a range with at most two segments never stops mid-way) ----
-    const int buf = kseg & 1;
-    if (kseg >= 2) {
+    // ---- hand this segment's per-warp state to a merge buffer; a CTA-wide
+    // barrier only when the buffer still holds an unmerged segment (with two
+    // buffers a range of at most two segments never stops mid-way) ----
+    const int buf = kseg % kBufs;
+    if (kseg >= kBufs) {
       consumer_bar();
       merge_buffer(buf);
       consumer_bar();
     }
     {
-      float* my = merge_bufs + buf * kMergeBufFloats + warp * kMaxGroup * kScratchStride;
-      float* bm = merge_bufs + buf * kMergeBufFloats + kScratchFloats;
-      float* bl = bm + kWarps * kMaxGroup;
+      float* base = merge_bufs + buf * Geom::kMergeBufFloats;
+      float* bm = base + Geom::kScratchFloats;
+      float* bl = bm + kWarps * kCols;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int d0 = 16 * g + 2 * i;
-        my[(2 * c) * kScratchStride + d0] = st.o[i][0];
-        my[(2 * c + 1) * kScratchStride + d0] = st.o[i][1];
-        my[(2 * c) * kScratchStride + d0 + 1] = st.o[i][2];
-        my[(2 * c + 1) * kScratchStride + d0 + 1] = st.o[i][3];
-      }
-      if (g == 0) {
-        bm[warp * kMaxGroup + 2 * c] = st.m0;
-        bm[warp * kMaxGroup + 2 * c + 1] = st.m1;
-        bl[warp * kMaxGroup + 2 * c] = st.l[0];
-        bl[warp * kMaxGroup + 2 * c + 1] = st.l[1];
+      for (int j = 0; j < NT; ++j) {
+        float* my = base + (warp * kCols + 8 * j) * kScratchStride;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int d0 = 16 * g + 2 * i;
+          my[(2 * c) * kScratchStride + d0] = st.o[j][i][0];
+          my[(2 * c + 1) * kScratchStride + d0] = st.o[j][i][1];
+          my[(2 * c) * kScratchStride + d0 + 1] = st.o[j][i][2];
+          my[(2 * c + 1) * kScratchStride + d0 + 1] = st.o[j][i][3];
+        }
+        if (g == 0) {
+          bm[warp * kCols + 8 * j + 2 * c] = st.m[j][0];
+          bm[warp * kCols + 8 * j + 2 * c + 1] = st.m[j][1];
+          bl[warp * kCols + 8 * j + 2 * c] = st.l[j][0];
+          bl[warp * kCols + 8 * j + 2 * c + 1] = st.l[j][1];
+        }
       }
       if (lane == 0) buf_poison[buf][warp] = poisoned;
       if (tid == 0) {
@@ -669,10 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ++s;
   }
 
-  // ---- merges still buffered (the range's last one or two segments) ----
+  // ---- merges still buffered (the range's last kBufs segments), in order ----
   consumer_bar();
-  if (kseg >= 2) merge_buffer(kseg & 1);
-  if (kseg >= 1) merge_buffer((kseg - 1) & 1);
+  for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k) merge_buffer(k % kBufs);
   consumer_bar();
 
   // ---- split pieces: flag, ticket, and merge by the CTA that finishes last ----
@@ -684,23 +748,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
     consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
     if (tid < npend) {
-      const int s = pend_seg[tid];
-      if (pend_poison[tid]) atomicOr(&p.seg_bad[s], 1);
+      const int ps = pend_seg[tid];
+      if (pend_poison[tid]) atomicOr(&p.seg_bad[ps], 1);
       int last = 0;
       if (p.fused_merge) {
-        const int ilo = cta_of_page(segs[s], total, n), ihi = cta_of_page(segs[s + 1] - 1, total, n);
+        const int ilo = cta_of_page(segs[ps], total, n), ihi = cta_of_page(segs[ps + 1] - 1, total, n);
         // release: this CTA's slots (ordered before by the barrier) are visible
         // to whoever takes a later ticket; acquire: the earlier pieces are
         // visible to this CTA after the next barrier
-        last = (atom_add_acq_rel_gpu(&p.seg_count[s], 1) == ihi - ilo) ? 1 : 0;
+        last = (atom_add_acq_rel_gpu(&p.seg_count[ps], 1) == ihi - ilo) ? 1 : 0;
       }
       pend_last[tid] = last;
     }
     consumer_bar();
     for (int i = 0; i < npend; ++i) {
       if (!pend_last[i]) continue;
-      const int s = pend_seg[i];
-      merge_pieces(p, s, segs[s], segs[s + 1], total, n, tid >> 5, (tid & 31) * 4, v_scale);
+      const int ps = pend_seg[i];
+      for (int col = tid >> 5; col < kCols; col += kWarps)
+        merge_pieces(p, ps, segs[ps], segs[ps + 1], total, n, col, (tid & 31) * 4, v_scale);
     }
   }
 
@@ -725,10 +790,11 @@ cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   // Programmatic dependent launch: CTAs may start while the planner (the
   // previous kernel on the stream) still runs; the kernel waits for it with
   // griddepcontrol.wait before reading or writing anything the planner writes.
+  const int nt = (p.group * p.q_len + 7) / 8;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_max);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kPartialSmem;
+  cfg.dynamicSmemBytes = nt == 1 ? PartialGeom<1>::kSmem : PartialGeom<2>::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -736,16 +802,19 @@ cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p.kv_dtype == XQA_KV_E4M3)
-    return cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3>, tm_k, tm_v, p);
-  return cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2>, tm_k, tm_v, p);
+    return nt == 1 ? cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 1>, tm_k, tm_v, p)
+                   : cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 2>, tm_k, tm_v, p);
+  return nt == 1 ? cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2, 1>, tm_k, tm_v, p)
+                 : cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2, 2>, tm_k, tm_v, p);
 }
 
 cudaError_t set_partial_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kPartialSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPartialSmem);
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2, 1>, a, PartialGeom<1>::kSmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 1>, a, PartialGeom<1>::kSmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2, 2>, a, PartialGeom<2>::kSmem)) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 2>, a, PartialGeom<2>::kSmem);
 }
 
 }  // namespace xqa

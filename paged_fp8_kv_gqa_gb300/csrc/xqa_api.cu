@@ -28,7 +28,7 @@ std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
 struct Resolved {
   int batch, hq, hkv, group, mbs, nb;
-  int nseg, n_max, min_pages, merge_mode, kv_dtype, kv_layout;
+  int nseg, n_max, min_pages, merge_mode, kv_dtype, kv_layout, q_len;
   float sm_scale;
   xqa::WsLayout ws;
 };
@@ -47,11 +47,13 @@ xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
   if (s->merge_mode != 0 && s->merge_mode != 1) return XQA_ERR_SHAPE;
   if (s->kv_dtype != XQA_KV_E5M2 && s->kv_dtype != XQA_KV_E4M3) return XQA_ERR_SHAPE;
   if (s->kv_layout != XQA_LAYOUT_HND && s->kv_layout != XQA_LAYOUT_NHD) return XQA_ERR_SHAPE;
+  const int q_len = s->q_len > 0 ? s->q_len : 1;
+  if (s->q_len < 0 || group * q_len > xqa::kMaxCols) return XQA_ERR_SHAPE;
   // int32 index arithmetic on the device: pool rows, total pages, segments
   const long long pool_rows = (long long)s->num_blocks * s->num_kv_heads * kBlockSize;
   const long long max_pages = (long long)s->batch * s->num_kv_heads * s->max_blocks_per_seq;
   if (pool_rows >= (1ll << 31) || max_pages >= (1ll << 31)) return XQA_ERR_SHAPE;
-  if ((long long)s->batch * s->num_q_heads >= (1ll << 31) / kHeadDim) return XQA_ERR_SHAPE;
+  if ((long long)s->batch * q_len * s->num_q_heads >= (1ll << 31) / kHeadDim) return XQA_ERR_SHAPE;
   r->batch = s->batch;
   r->hq = s->num_q_heads;
   r->hkv = s->num_kv_heads;
@@ -64,6 +66,7 @@ xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
   r->merge_mode = s->merge_mode;
   r->kv_dtype = s->kv_dtype;
   r->kv_layout = s->kv_layout;
+  r->q_len = q_len;
   if (s->max_ctas > 0) {
     r->n_max = s->max_ctas;
   } else {
@@ -206,6 +209,7 @@ xqa_status_t attend_partial_impl(const void* q, const uint8_t* k_cache, const ui
   p.num_blocks = r.nb;
   p.kv_dtype = r.kv_dtype;
   p.kv_layout = r.kv_layout;
+  p.q_len = r.q_len;
   p.qk_scale_base = (double)r.sm_scale * 1.4426950408889634;  // sm_scale * log2(e)
   p.k_scale = k_scale;
   p.v_scale = v_scale;
@@ -235,6 +239,7 @@ xqa_status_t combine_impl(const int32_t* context_lens, float v_scale, const floa
   p.num_q_heads = r.hq;
   p.num_kv_heads = r.hkv;
   p.group = r.group;
+  p.q_len = r.q_len;
   p.v_scale = v_scale;
   p.v_scale_ptr = v_scale_ptr;
   cudaError_t e = xqa::launch_combine(p, r.nseg, (cudaStream_t)stream);

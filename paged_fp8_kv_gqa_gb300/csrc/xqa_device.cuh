@@ -17,6 +17,7 @@ namespace xqa {
 constexpr int kHeadDim = 128;
 constexpr int kBlockSize = 16;
 constexpr int kMaxGroup = 8;                                  // q heads per kv head (MMA N = 8)
+constexpr int kMaxCols = 16;  // columns (new token x head) per kv head: G * q_len <= 16
 constexpr int kPageBytes = kBlockSize * kHeadDim;             // one (page, kv head) slice: 2048 B
 constexpr int kStageBytes = 2 * kPageBytes;                   // K slice + V slice
 constexpr int kWarps = 8;                                     // every warp loads and computes
@@ -24,20 +25,32 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 32;                                   // smem ring depth (multiple of kWarps)
 constexpr int kLookahead = kStages / kWarps;                  // pages in flight per warp
 constexpr int kScratchStride = kHeadDim + 4;                  // floats per (warp, head) merge row
-constexpr int kScratchFloats = kWarps * kMaxGroup * kScratchStride;
-// one merge buffer: every warp's O rows, then m[warp][head], l[warp][head]
-constexpr int kMergeBufFloats = kScratchFloats + 2 * kWarps * kMaxGroup;
-constexpr int kMergeBufs = 2;  // segments whose merge may be pending at once
 constexpr int kSegCache = 2048;                               // seg_start entries kept in smem
-constexpr int kPartialSmem =
-    1024 /* alignment slack for the 1024-B swizzle atom */ + kStages * kStageBytes +
-    kMergeBufs * kMergeBufFloats * 4 + kSegCache * 4;
+
+// Per-instance geometry of the partial kernel with NT MMA column tiles
+// (8 * NT columns = new token x head): merge buffers hold every warp's O rows,
+// then m[warp][col], l[warp][col]. One-tile kernels keep two buffers (merges
+// deferred), two-tile kernels one (their buffer is twice as large).
+template <int NT>
+struct PartialGeom {
+  static constexpr int kCols = 8 * NT;
+  static constexpr int kScratchFloats = kWarps * kCols * kScratchStride;
+  static constexpr int kMergeBufFloats = kScratchFloats + 2 * kWarps * kCols;
+  static constexpr int kMergeBufs = NT == 1 ? 2 : 1;
+  static constexpr int kSmem = 1024 /* alignment slack for the 1024-B swizzle atom */ +
+                               kStages * kStageBytes + kMergeBufs * kMergeBufFloats * 4 +
+                               kSegCache * 4;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
 constexpr int kDefaultMinPagesPerCta = 8;
 constexpr int kPlanThreads = 256;  // small enough to share an SM with a partial CTA
 constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
 
-// Partial-result slot: O[8][128] unnormalised fp32, then M[8] (log2 domain), L[8].
-constexpr int kSlotFloats = kMaxGroup * kHeadDim + 2 * kMaxGroup;
+// Partial-result slot: O[col][128] unnormalised fp32, then M[col] (log2 domain),
+// L[col], for up to kMaxCols columns.
+constexpr int kSlotFloats = kMaxCols * kHeadDim + 2 * kMaxCols;
+constexpr int kSlotM = kMaxCols * kHeadDim;
+constexpr int kSlotL = kMaxCols * kHeadDim + kMaxCols;
 
 // A pipeline wait that has not completed after this long is treated as a fault.
 constexpr unsigned long long kWaitBudgetNs = 1000000000ull;  // 1 s

@@ -18,6 +18,7 @@ struct PartialParams {
   int32_t* seg_count;        // [nseg] pieces finished (in-kernel merge tickets)
   float* partials;           // [(n_max + nseg) * kSlotFloats]
   int batch, num_q_heads, num_kv_heads, group, max_blocks_per_seq, num_blocks;
+  int q_len;                 // new tokens per sequence (q, out: [B, q_len, Hq, D])
   int n_max, min_pages;      // split rule inputs (same values the planner got)
   int fused_merge;           // 1: the last CTA of a split segment merges it
   int kv_dtype, kv_layout;   // XQA_KV_* code format, XQA_LAYOUT_* cache layout
@@ -33,7 +34,7 @@ struct CombineParams {
   const int32_t* seg_start;
   const int32_t* seg_bad;
   const float* partials;
-  int num_q_heads, num_kv_heads, group;
+  int num_q_heads, num_kv_heads, group, q_len;
   float v_scale;
   const float* v_scale_ptr;  // optional device scalar (overrides v_scale)
 };

@@ -27,9 +27,9 @@ def oracle_out(name: str) -> np.ndarray:
 
 
 def oracle_of(w: wl.Workload, sm_scale=None) -> np.ndarray:
-    return attention.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables,
-                                            w.context_lens, w.k_scale, w.v_scale, sm_scale,
-                                            kv_dtype=w.kv_dtype, kv_layout=w.kv_layout)
+    fn = attention.paged_decode_attention_multi if w.q.ndim == 4 else attention.paged_decode_attention
+    return fn(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.k_scale, w.v_scale,
+              sm_scale, kv_dtype=w.kv_dtype, kv_layout=w.kv_layout)
 
 
 def to_dev(a: np.ndarray) -> torch.Tensor:

@@ -54,7 +54,7 @@ def test_host_validation_without_device(lib):
     nseg = 64
     head = 16 + 4 * (nseg + 1) + 4 * nseg + 4 * nseg
     head = (head + 255) // 256 * 256
-    assert n.value == head + (152 + nseg) * (8 * 128 + 16) * 4
+    assert n.value == head + (152 + nseg) * (16 * 128 + 32) * 4
     for bad in (
         xqa.XqaShape(16, 32, 4, 64, 16, 1200, 22240, 0.0, 152, 0),   # head_dim
         xqa.XqaShape(16, 32, 4, 128, 32, 1200, 22240, 0.0, 152, 0),  # block size
@@ -63,6 +63,9 @@ def test_host_validation_without_device(lib):
         xqa.XqaShape(0, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0),   # batch
         xqa.XqaShape(16, 32, 4, 128, 16, 1200, 2**28, 0.0, 152, 0),  # pool too large for int32 rows
         xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0, 2),  # merge mode
+        xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0, 0, 2),  # kv dtype
+        xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0, 0, 0, 2),  # kv layout
+        xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0, 0, 0, 0, 3),  # G * T > 16
     ):
         assert lib.xqa_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == xqa.XQA_ERR_SHAPE
     assert lib.xqa_workspace_size(None, ctypes.byref(n)) == xqa.XQA_ERR_NULL
