@@ -240,7 +240,7 @@ def run_gpu(args, world, rank, local, dist):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = workloads.make_workload(args.workload, kv_dtype=args.kv_dtype)
+    w = workloads.make_workload(args.workload, kv_dtype=args.kv_dtype, q_len=args.q_len)
     if args.kv_layout == "nhd":
         w = workloads.to_nhd(w)
     kv_bytes = w.kv_bytes
@@ -428,6 +428,7 @@ def run_gpu(args, world, rank, local, dist):
             "merge_mode": shape.merge_mode,
             "kv_dtype": args.kv_dtype,
             "kv_layout": args.kv_layout,
+            "q_len": args.q_len,
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "pct_of_nominal_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
@@ -547,6 +548,7 @@ def main(argv=None):
                     help="bracket every n-th step of the timed graph with CUDA events")
     ap.add_argument("--kv-dtype", choices=("e5m2", "e4m3"), default="e5m2")
     ap.add_argument("--kv-layout", choices=("hnd", "nhd"), default="hnd")
+    ap.add_argument("--q-len", type=int, default=1, help="new tokens per sequence")
     ap.add_argument("--merge-mode", type=int, choices=(0, 1), default=0,
                     help="0: split segments merged inside the partial kernel; 1: combine kernel")
     ap.add_argument("--warm-seconds", type=float, default=1.0)
