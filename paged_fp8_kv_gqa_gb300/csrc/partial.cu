@@ -57,6 +57,11 @@ namespace xqa {
 namespace {
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Running-max start value: finite, so a column that has seen no visible token
+// yet needs no special case: 2^(-inf - kNoMax) = 0 for its masked logits, its
+// rescale factor stays 2^0 = 1, and the first real maximum rescales its
+// all-zero state by 2^(kNoMax - m) = 0.
+constexpr float kNoMax = -1e30f;
 constexpr uint32_t kOnesHalf2 = 0x3C003C00u;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -151,7 +156,7 @@ __device__ __forceinline__ void reset_state(WarpState<NT>& st) {
       for (int k = 0; k < 4; ++k) st.o[j][i][k] = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) st.l[j][k] = 0.f;
-    st.m[j][0] = st.m[j][1] = -INFINITY;
+    st.m[j][0] = st.m[j][1] = kNoMax;
   }
 }
 
@@ -191,7 +196,7 @@ struct SegLimits {
 // every column tile, one online-softmax update, PV for every tile. The V
 // fragments are converted once and shared by all tiles. With two pages the two
 // independent chains interleave and hide each other's fixed latencies.
-template <int kFmt, int NP, int NT>
+template <int kFmt, int NP, int NT, bool kMulti>
 __device__ __forceinline__ void process_pages(WarpState<NT>& st, const PageRegs (&r)[NP],
                                               const uint32_t (&qf)[NT][16], const int (&tok0)[NP],
                                               const int (&nvalid)[NP], const SegLimits<NT>& sl,
@@ -231,7 +236,12 @@ __device__ __forceinline__ void process_pages(WarpState<NT>& st, const PageRegs 
     for (int j = 0; j < NT; ++j) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) t[pi][j][k] = s[pi][j][k] * scale_log2;
-      if (masked) {
+      if (!kMulti) {  // one new token: every column's limit is ctx - 1
+        if (nvalid[pi] < kBlockSize) {
+          if (g >= nvalid[pi]) t[pi][j][0] = t[pi][j][1] = -INFINITY;
+          if (g + 8 >= nvalid[pi]) t[pi][j][2] = t[pi][j][3] = -INFINITY;
+        }
+      } else if (masked) {
         if (r0 > sl.lim[j][0]) t[pi][j][0] = -INFINITY;
         if (r0 > sl.lim[j][1]) t[pi][j][1] = -INFINITY;
         if (r1 > sl.lim[j][0]) t[pi][j][2] = -INFINITY;
@@ -257,9 +267,7 @@ __device__ __forceinline__ void process_pages(WarpState<NT>& st, const PageRegs 
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float nm = fmaxf(st.m[j][e], mx[j][e]);
-        // a column that has seen no visible token yet keeps max -inf and an
-        // all-zero state: its rescale factor is 1, not 2^(-inf - -inf)
-        const float a = (nm == -INFINITY) ? 1.f : ex2(st.m[j][e] - nm);
+        const float a = ex2(st.m[j][e] - nm);
         st.m[j][e] = nm;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -278,10 +286,8 @@ __device__ __forceinline__ void process_pages(WarpState<NT>& st, const PageRegs 
     uint32_t pb0[NT], pb1[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const float m0 = st.m[j][0] == -INFINITY ? 0.f : st.m[j][0];
-      const float m1 = st.m[j][1] == -INFINITY ? 0.f : st.m[j][1];
-      const float p0 = ex2(t[pi][j][0] - m0), p1 = ex2(t[pi][j][1] - m1);
-      const float p2 = ex2(t[pi][j][2] - m0), p3 = ex2(t[pi][j][3] - m1);
+      const float p0 = ex2(t[pi][j][0] - st.m[j][0]), p1 = ex2(t[pi][j][1] - st.m[j][1]);
+      const float p2 = ex2(t[pi][j][2] - st.m[j][0]), p3 = ex2(t[pi][j][3] - st.m[j][1]);
       pb0[j] = movmatrix_trans(pack_half2(p0, p1));
       pb1[j] = movmatrix_trans(pack_half2(p2, p3));
     }
@@ -385,7 +391,7 @@ __device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int 
 
 }  // namespace
 
-template <int kFmt, int NT>
+template <int kFmt, int NT, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1)
     partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const PartialParams p) {
@@ -676,18 +682,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nv0 = min(kBlockSize, ctx - t0), nv1 = min(kBlockSize, ctx - t1);
       if (kPairs && pair && !bad0 && !bad1) {
         const int tk[2] = {t0, t1}, nv[2] = {nv0, nv1};
-        process_pages<kFmt, 2, NT>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
+        process_pages<kFmt, 2, NT, kMulti>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
       } else {
         if (bad0 || bad1) poisoned = 1;
         if (!bad0) {
           const PageRegs one[1] = {regs[0]};
           const int tk[1] = {t0}, nv[1] = {nv0};
-          process_pages<kFmt, 1, NT>(st, one, qf, tk, nv, sl, scale_log2, g, c);
+          process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
         }
         if (pair && !bad1) {
           const PageRegs one[1] = {regs[1]};
           const int tk[1] = {t1}, nv[1] = {nv1};
-          process_pages<kFmt, 1, NT>(st, one, qf, tk, nv, sl, scale_log2, g, c);
+          process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
         }
       }
     }
@@ -801,20 +807,29 @@ cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.kv_dtype == XQA_KV_E4M3)
-    return nt == 1 ? cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 1>, tm_k, tm_v, p)
-                   : cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 2>, tm_k, tm_v, p);
-  return nt == 1 ? cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2, 1>, tm_k, tm_v, p)
-                 : cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2, 2>, tm_k, tm_v, p);
+  // instances: (format) x (one tile, single token | one tile, several tokens |
+  // two tiles)
+  const bool multi = p.q_len > 1;
+  if (p.kv_dtype == XQA_KV_E4M3) {
+    if (nt == 2) return cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 2, true>, tm_k, tm_v, p);
+    return multi ? cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 1, true>, tm_k, tm_v, p)
+                 : cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 1, false>, tm_k, tm_v, p);
+  }
+  if (nt == 2) return cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2, 2, true>, tm_k, tm_v, p);
+  return multi ? cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2, 1, true>, tm_k, tm_v, p)
+               : cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E5M2, 1, false>, tm_k, tm_v, p);
 }
 
 cudaError_t set_partial_attributes() {
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  const int s1 = PartialGeom<1>::kSmem, s2 = PartialGeom<2>::kSmem;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2, 1>, a, PartialGeom<1>::kSmem)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 1>, a, PartialGeom<1>::kSmem)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2, 2>, a, PartialGeom<2>::kSmem)) != cudaSuccess) return e;
-  return cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 2>, a, PartialGeom<2>::kSmem);
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2, 1, false>, a, s1)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2, 1, true>, a, s1)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2, 2, true>, a, s2)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 1, false>, a, s1)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 1, true>, a, s1)) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 2, true>, a, s2);
 }
 
 }  // namespace xqa
