@@ -33,8 +33,9 @@
 //   - O^T[128 x 8] += V^T * P^T with 8 MMAs per tile (V converted once for all
 //     tiles) plus one MMA against ones for the row sums l (so l sums exactly
 //     the fp16 P used for O).
-// With one tile a warp takes its pages two at a time, interleaving two
-// independent dependency chains. At the end of a segment each warp hands its
+// A warp takes its pages two at a time, interleaving two independent
+// dependency chains (two-tile kernels load Q per segment instead of
+// prefetching it, to stay within 255 registers). At the end of a segment each warp hands its
 // (m, l, O) to a shared merge buffer and moves on; the buffered segments are
 // merged across warps when a buffer is reused and at the end of the range. A
 // segment owned whole by this CTA is normalised and written as fp16
@@ -192,7 +193,7 @@ struct SegLimits {
   int min_lim;
 };
 
-// NP 16-token pages (NP = 2 only with one column tile) of one kv head: QK for
+// NP (1 or 2) 16-token pages of one kv head: QK for
 // every column tile, one online-softmax update, PV for every tile. The V
 // fragments are converted once and shared by all tiles. With two pages the two
 // independent chains interleave and hide each other's fixed latencies.
@@ -398,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Geom = PartialGeom<NT>;
   constexpr int kCols = Geom::kCols;
   constexpr int kBufs = Geom::kMergeBufs;
-  constexpr bool kPairs = NT == 1;  // two pages per warp iteration
+  constexpr bool kPairs = true;  // two pages per warp iteration
+  constexpr bool kPrefetchQ = NT == 1;  // registers: two-tile kernels load Q per segment
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ int stage_bad[kStages];
@@ -625,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = s / p.num_kv_heads;
     const int ctx = __ldg(&p.context_lens[b]);
     const bool whole = (sb >= cbeg) && (se <= cend);
-    if (q_next_seg == s) {
+    if (kPrefetchQ && q_next_seg == s) {
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -633,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       load_q<NT>(p, s, g, c, qf);
     }
-    if (qe < npages) {  // prefetch Q of the next segment this CTA works on
+    if (kPrefetchQ && qe < npages) {  // prefetch Q of the next segment this CTA works on
       q_next_seg = find_segment(segs, s, nseg, cbeg + qe);
       load_q<NT>(p, q_next_seg, g, c, qf_next);
     }
