@@ -166,6 +166,14 @@ xqa_status_t xqa_dequant_e5m2(const uint8_t* in, size_t n, float scale, uint16_t
 xqa_status_t xqa_dequant_e4m3(const uint8_t* in, size_t n, float scale, uint16_t* out_fp16_bits,
                               float* out_f32, void* stream);
 
+/* Self-check of the device-side failure detection: launches one CTA whose
+ * threads wait, through the same bounded mbarrier wait the attention kernel
+ * uses, on a barrier that nothing ever arrives at. After budget_ns
+ * (1 .. 2e9 ns) the wait gives up and the kernel writes XQA_ERR_DEVICE_TIMEOUT
+ * to *device_status (a device int32) and returns; the context stays usable.
+ * The attention kernel's budget is 1 s. Test use only. */
+xqa_status_t xqa_selftest_wait_timeout(int32_t* device_status, uint64_t budget_ns, void* stream);
+
 /* Copies the workspace status word to *device_status (an xqa_status_t value:
  * XQA_OK or one of the device-reported codes). Synchronises `stream`. */
 xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void* stream);

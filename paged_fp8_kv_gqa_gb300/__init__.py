@@ -45,6 +45,7 @@ EXPORTED = (
     "xqa_decode_static_workspace",
     "xqa_decode_device_scales",
     "xqa_dequant_e4m3",
+    "xqa_selftest_wait_timeout",
 )
 
 KV_DTYPES = {"e5m2": 0, "e4m3": 1}
@@ -97,6 +98,7 @@ _SIGS = {
     "xqa_decode_static_workspace": [_P, _P, _P, _P, _P, _F, _F, _P, _SHAPE, _P],
     "xqa_decode_device_scales": [_P, _P, _P, _P, _P, _P, _P, _P, _SHAPE, _P, _SZ, _P],
     "xqa_dequant_e4m3": [_P, _SZ, _F, _P, _P, _P],
+    "xqa_selftest_wait_timeout": [_P, ctypes.c_uint64, _P],
 }
 
 
@@ -308,3 +310,14 @@ def xqa_decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens,
         ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], float(k_scale), float(v_scale), ptrs[5],
         ctypes.byref(shape), _stream_handle(stream)), "xqa_decode_static_workspace")
     return out
+
+
+def xqa_selftest_wait_timeout(budget_ns: int, stream=None) -> int:
+    """Run the bounded-wait self-check (a wait nothing completes); returns the
+    status the kernel wrote (XQA_ERR_DEVICE_TIMEOUT when the wait gave up)."""
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check(load_library().xqa_selftest_wait_timeout(status.data_ptr(), int(budget_ns),
+                                                    _stream_handle(stream)),
+           "xqa_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    return int(status.item())

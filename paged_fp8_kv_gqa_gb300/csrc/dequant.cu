@@ -53,6 +53,30 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ in, size_t n, float s
   }
 }
 
+// Self-check of the bounded pipeline wait: every thread waits on an mbarrier
+// that nothing arrives at, with the given budget; the wait must give up and
+// the kernel must record XQA_ERR_DEVICE_TIMEOUT and return. No copy is in
+// flight, so leaving the barrier incomplete is harmless.
+__global__ void wait_timeout_kernel(int32_t* status, unsigned long long budget_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int never;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    never = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool done = mbar_wait_bounded(&bar, 0, &never, budget_ns);
+  if (!done && threadIdx.x == 0) atomicExch(status, XQA_ERR_DEVICE_TIMEOUT);
+  if (done && threadIdx.x == 0) atomicExch(status, XQA_OK);
+}
+
+cudaError_t launch_wait_timeout(int32_t* status, unsigned long long budget_ns,
+                                cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 64, 0, stream>>>(status, budget_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dequant(int kv_dtype, const uint8_t* in, size_t n, float scale,
                            uint16_t* out16, float* out32, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;

@@ -328,6 +328,14 @@ xqa_status_t xqa_dequant_e4m3(const uint8_t* in, size_t n, float scale, uint16_t
   return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
 }
 
+xqa_status_t xqa_selftest_wait_timeout(int32_t* device_status, uint64_t budget_ns,
+                                       void* stream) {
+  if (!device_status) return XQA_ERR_NULL;
+  if (budget_ns == 0 || budget_ns > 2000000000ull) return XQA_ERR_SHAPE;
+  cudaError_t e = xqa::launch_wait_timeout(device_status, budget_ns, (cudaStream_t)stream);
+  return e == cudaSuccess ? XQA_OK : XQA_ERR_LAUNCH;
+}
+
 xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void* stream) {
   if (!workspace || !device_status) return XQA_ERR_NULL;
   cudaStream_t s = (cudaStream_t)stream;

@@ -123,9 +123,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of `bar`. Gives up (returns false) when *abort is
-// set by another warp or after kWaitBudgetNs; never spins without bound.
+// set by another warp or after budget_ns; never spins without bound.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort) {
+                                                  volatile int* abort,
+                                                  uint64_t budget_ns = kWaitBudgetNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
@@ -133,7 +134,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitBudgetNs) return false;
+    if (global_timer_ns() - t0 > budget_ns) return false;
   }
 }
 

@@ -45,6 +45,8 @@ cudaError_t launch_plan(const int32_t* context_lens, int batch, int num_kv_heads
 cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const PartialParams& p, int n_max, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int num_segments, cudaStream_t stream);
+cudaError_t launch_wait_timeout(int32_t* status, unsigned long long budget_ns,
+                                cudaStream_t stream);
 cudaError_t launch_dequant(int kv_dtype, const uint8_t* in, size_t n, float scale,
                            uint16_t* out16, float* out32, cudaStream_t stream);
 
