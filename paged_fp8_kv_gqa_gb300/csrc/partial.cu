@@ -418,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
+  griddep_launch_dependents();  // a dependent next kernel waits for this grid itself
   const int nseg = p.batch * p.num_kv_heads;
   const int ncols = p.group * p.q_len;
   // per-tensor scales: host values, or device scalars read when the kernel runs
@@ -429,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* merge_bufs = reinterpret_cast<float*>(stages + kStages * kStageBytes);
   int32_t* seg_cache = reinterpret_cast<int32_t*>(merge_bufs + kBufs * Geom::kMergeBufFloats);
+  int32_t* ctx_cache = seg_cache + kSegCache;  // context length per sequence
 
   // ---- the plan: computed here when the segment table fits in shared memory
   // (same integer rule as the planner kernel), else read from the planner ----
@@ -444,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pages = 0;
       if (b < p.batch) {
         const int ctx = __ldg(&p.context_lens[b]);
+        ctx_cache[b] = ctx;
         pages = (ctx < 0 || (long long)ctx > max_ctx) ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
       }
       int incl = pages;
@@ -625,7 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sb = segs[s], se = segs[s + 1];
     const int qe = min(se, cend) - cbeg;
     const int b = s / p.num_kv_heads;
-    const int ctx = __ldg(&p.context_lens[b]);
+    // from shared memory when the plan was computed here: no global round trip
+    // at a segment switch
+    const int ctx = segs_in_smem ? ctx_cache[b] : __ldg(&p.context_lens[b]);
     const bool whole = (sb >= cbeg) && (se <= cend);
     if (kPrefetchQ && q_next_seg == s) {
 #pragma unroll

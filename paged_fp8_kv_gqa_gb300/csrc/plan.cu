@@ -12,7 +12,10 @@
 // plan is computed on the device so the decode step needs no host sync. It also
 // resets the status word, the bad-segment flags and the per-segment piece
 // counters of the in-kernel merge; the partial kernel, launched as its
-// programmatic dependent, waits for it before touching any of them.
+// programmatic dependent, waits for it before touching any of them. The
+// planner is itself launched as a programmatic dependent of the previous
+// kernel on the stream: it becomes resident early and waits for that kernel to
+// complete before it reads or writes anything.
 #include "xqa_device.cuh"
 #include "xqa_launch.h"
 
@@ -32,6 +35,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             int batch, int num_kv_heads,
                                                             int max_blocks_per_seq, int n_max,
                                                             int min_pages, int32_t* ws) {
+  griddep_wait();               // everything earlier on the stream is complete
   griddep_launch_dependents();  // the partial kernel may start its prologue now
   const int nseg = batch * num_kv_heads;
   int32_t* header = ws;
@@ -85,10 +89,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 cudaError_t launch_plan(const int32_t* context_lens, int batch, int num_kv_heads,
                         int max_blocks_per_seq, int n_max, int min_pages_per_cta,
                         int32_t* workspace, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(context_lens, batch, num_kv_heads,
-                                              max_blocks_per_seq, n_max, min_pages_per_cta,
-                                              workspace);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, context_lens, batch, num_kv_heads,
+                            max_blocks_per_seq, n_max, min_pages_per_cta, workspace);
 }
 
 }  // namespace xqa

@@ -25,7 +25,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 32;                                   // smem ring depth (multiple of kWarps)
 constexpr int kLookahead = kStages / kWarps;                  // pages in flight per warp
 constexpr int kScratchStride = kHeadDim + 4;                  // floats per (warp, head) merge row
-constexpr int kSegCache = 2048;                               // seg_start entries kept in smem
+constexpr int kSegCache = 2048;  // seg_start (and context length) entries kept in smem
 
 // Per-instance geometry of the partial kernel with NT MMA column tiles
 // (8 * NT columns = new token x head): merge buffers hold every warp's O rows,
@@ -39,7 +39,7 @@ struct PartialGeom {
   static constexpr int kMergeBufs = NT == 1 ? 2 : 1;
   static constexpr int kSmem = 1024 /* alignment slack for the 1024-B swizzle atom */ +
                                kStages * kStageBytes + kMergeBufs * kMergeBufFloats * 4 +
-                               kSegCache * 4;
+                               kSegCache * 4 /* segment starts */ + kSegCache * 4 /* lengths */;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 constexpr int kDefaultMinPagesPerCta = 8;
