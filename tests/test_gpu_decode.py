@@ -197,6 +197,32 @@ def test_cuda_graph_replay_with_changed_inputs():
     assert_close(replayed, oracle_of(w2), "graph replay")
 
 
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_inputs_written_by_the_previous_kernel_are_seen(merge_mode):
+    # q and the context lengths are rewritten by ordinary kernels on the same
+    # stream right before every decode, with no synchronisation in between: the
+    # planner (a programmatic dependent of whatever ran before) must wait for
+    # those kernels before the partial kernel reads anything
+    w = wl.make_custom([700, 33, 5000, 2049], 32, 4, seed=61)
+    w2 = w.copy()
+    w2.q = -w.q
+    w2.context_lens = np.array([650, 1, 4000, 17], dtype=np.int32)
+    refs = [oracle_of(w), oracle_of(w2)]
+    d = Dev(w, merge_mode=merge_mode)
+    srcs = [(to_dev(w.q), to_dev(w.context_lens)), (to_dev(w2.q), to_dev(w2.context_lens))]
+    outs = []
+    for it in range(12):
+        q_src, lens_src = srcs[it % 2]
+        torch.mul(q_src, 1.0, out=d.q)
+        torch.add(lens_src, 0, out=d.lens)
+        d.run()
+        outs.append(d.out.clone())
+    torch.cuda.synchronize()
+    assert d.status() == xqa.XQA_OK
+    for it, o in enumerate(outs):
+        assert_close(o.cpu().numpy(), refs[it % 2], f"iteration {it}")
+
+
 # --------------------------------------------------------------------------
 # error paths
 # --------------------------------------------------------------------------
