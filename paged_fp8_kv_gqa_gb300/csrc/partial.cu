@@ -328,66 +328,83 @@ __device__ __forceinline__ void store_half4(__half* o, float a, float b, float c
   *reinterpret_cast<uint2*>(o) = v;
 }
 
-// LSE merge of all pieces of split segment s into fp16 rows (thread: column
-// col, dims dq..dq+3). Pieces were written by other CTAs: read through L2.
-__device__ __forceinline__ void merge_pieces(const PartialParams& p, int s, int sb, int se,
-                                             int total, int n, int col, int dq, float v_scale) {
+// LSE merge of the split segments this CTA completed (at most two: the first
+// and the last of its range) into fp16 rows, thread: column col, dims
+// dq..dq+3. Pieces were written by other CTAs: read through L2. The bad flags
+// and, for segments of at most kFew pieces, every piece of both segments are
+// loaded before any is used (one round trip for the whole merge).
+__device__ __forceinline__ void merge_segments(const PartialParams& p, const int (&ms)[2], int nm,
+                                               const int32_t* segs, int total, int n, int col,
+                                               int dq, float v_scale) {
   if (col >= p.group * p.q_len) return;
-  const int ilo = cta_of_page(sb, total, n), ihi = cta_of_page(se - 1, total, n);
-  __half* o = p.out + col_row(p, s, col) * kHeadDim + dq;
-  if (__ldcg(&p.seg_bad[s]) != 0) {
-    const float nan = __int_as_float(0x7fc00000);
-    store_half4(o, nan, nan, nan, nan);
-    return;
-  }
-  float M = -INFINITY;
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int kFew = 4;
-  if (ihi - ilo < kFew) {
-    // usual case: every load issued before any is used (one L2 round trip)
-    float mi[kFew], li[kFew];
-    float4 oi[kFew];
+  int ilo[2], ihi[2], bad[2];
+  float mi[2][kFew], li[2][kFew];
+  float4 oi[2][kFew];
 #pragma unroll
-    for (int k = 0; k < kFew; ++k) {
-      if (ilo + k <= ihi) {
-        const float* slot = p.partials + (size_t)(ilo + k + s) * kSlotFloats;
-        mi[k] = __ldcg(slot + kSlotM + col);
-        li[k] = __ldcg(slot + kSlotL + col);
-        oi[k] = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
+  for (int j = 0; j < 2; ++j) {
+    if (j < nm) {
+      const int s = ms[j];
+      ilo[j] = cta_of_page(segs[s], total, n);
+      ihi[j] = cta_of_page(segs[s + 1] - 1, total, n);
+      bad[j] = __ldcg(&p.seg_bad[s]);
+#pragma unroll
+      for (int k = 0; k < kFew; ++k) {
+        if (ilo[j] + k <= ihi[j]) {
+          const float* slot = p.partials + (size_t)(ilo[j] + k + s) * kSlotFloats;
+          mi[j][k] = __ldcg(slot + kSlotM + col);
+          li[j][k] = __ldcg(slot + kSlotL + col);
+          oi[j][k] = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
+        }
       }
-    }
-#pragma unroll
-    for (int k = 0; k < kFew; ++k)
-      if (ilo + k <= ihi) M = fmaxf(M, mi[k]);
-#pragma unroll
-    for (int k = 0; k < kFew; ++k) {
-      if (ilo + k <= ihi) {
-        const float w = (mi[k] == -INFINITY) ? 0.f : ex2(mi[k] - M);
-        L += w * li[k];
-        acc.x += w * oi[k].x;
-        acc.y += w * oi[k].y;
-        acc.z += w * oi[k].z;
-        acc.w += w * oi[k].w;
-      }
-    }
-  } else {
-    for (int i = ilo; i <= ihi; ++i)
-      M = fmaxf(M, __ldcg(p.partials + (size_t)(i + s) * kSlotFloats + kSlotM + col));
-    for (int i = ilo; i <= ihi; ++i) {
-      const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
-      const float mi = __ldcg(slot + kSlotM + col);
-      const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
-      L += w * __ldcg(slot + kSlotL + col);
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
-      acc.x += w * x.x;
-      acc.y += w * x.y;
-      acc.z += w * x.z;
-      acc.w += w * x.w;
     }
   }
-  const float rr = (L > 0.f) ? v_scale / L : 0.f;  // a new token with no visible token: 0
-  store_half4(o, acc.x * rr, acc.y * rr, acc.z * rr, acc.w * rr);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    if (j >= nm) continue;
+    const int s = ms[j];
+    __half* o = p.out + col_row(p, s, col) * kHeadDim + dq;
+    if (bad[j] != 0) {
+      const float nan = __int_as_float(0x7fc00000);
+      store_half4(o, nan, nan, nan, nan);
+      continue;
+    }
+    float M = -INFINITY;
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ihi[j] - ilo[j] < kFew) {
+#pragma unroll
+      for (int k = 0; k < kFew; ++k)
+        if (ilo[j] + k <= ihi[j]) M = fmaxf(M, mi[j][k]);
+#pragma unroll
+      for (int k = 0; k < kFew; ++k) {
+        if (ilo[j] + k <= ihi[j]) {
+          const float w = (mi[j][k] == -INFINITY) ? 0.f : ex2(mi[j][k] - M);
+          L += w * li[j][k];
+          acc.x += w * oi[j][k].x;
+          acc.y += w * oi[j][k].y;
+          acc.z += w * oi[j][k].z;
+          acc.w += w * oi[j][k].w;
+        }
+      }
+    } else {  // many pieces (small shares): two passes through L2
+      for (int i = ilo[j]; i <= ihi[j]; ++i)
+        M = fmaxf(M, __ldcg(p.partials + (size_t)(i + s) * kSlotFloats + kSlotM + col));
+      for (int i = ilo[j]; i <= ihi[j]; ++i) {
+        const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
+        const float m = __ldcg(slot + kSlotM + col);
+        const float w = (m == -INFINITY) ? 0.f : ex2(m - M);
+        L += w * __ldcg(slot + kSlotL + col);
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
+      }
+    }
+    const float rr = (L > 0.f) ? v_scale / L : 0.f;  // a new token with no visible token: 0
+    store_half4(o, acc.x * rr, acc.y * rr, acc.z * rr, acc.w * rr);
+  }
 }
 
 }  // namespace
@@ -774,12 +791,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       pend_last[tid] = last;
     }
     consumer_bar();
+    int m0 = 0, m1 = 0, nm = 0;  // the segments this CTA completes (at most two)
     for (int i = 0; i < npend; ++i) {
       if (!pend_last[i]) continue;
-      const int ps = pend_seg[i];
-      for (int col = tid >> 5; col < kCols; col += kWarps)
-        merge_pieces(p, ps, segs[ps], segs[ps + 1], total, n, col, (tid & 31) * 4, v_scale);
+      if (nm == 0) m0 = pend_seg[i];
+      else m1 = pend_seg[i];
+      ++nm;
     }
+    const int ms[2] = {m0, m1};
+    if (nm > 0)
+      for (int col = tid >> 5; col < kCols; col += kWarps)
+        merge_segments(p, ms, nm, segs, total, n, col, (tid & 31) * 4, v_scale);
   }
 
   // Drain: after an abort some issued copies may not have been waited for; every
