@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 METRIC = "decode-attn µs/step and KV GB/s (% of GB300 HBM peak), B16 ragged ~17.8K ctx"
 DEFAULT_WORKLOAD = "b16_ragged_ctx16384_19200"
 FALLBACK_HBM_GBS = 6800.0
+REPEATS = 5  # chunks of the timed region for the per-step spread
 NOMINAL_HBM_GBS = 8000.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "partial_kernel_b16_ragged.md")
 KERNEL_SOURCES = ("paged_fp8_kv_gqa_gb300/csrc/partial.cu", "paged_fp8_kv_gqa_gb300/csrc/xqa_device.cuh")
@@ -203,20 +204,43 @@ print(json.dumps({{"median_s": times[len(times)//2], "runs": n, "kv_bytes": w.kv
 """
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, else implementer/part)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model name"):
+        for line in info:
+            if line.startswith(key):
+                return line.split(":", 1)[1].strip()
+    fields = {}
+    for line in info:
+        if ":" in line:
+            k, v = (x.strip() for x in line.split(":", 1))
+            fields.setdefault(k, v)
+    if "CPU implementer" in fields:
+        return f"implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return "unknown"
+
+
 def cpu_baseline(name: str, budget_s: float = 12.0):
-    """The float64 oracle on the whole workload, single-threaded, in a fresh process."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    """The float64 oracle on the whole workload as it stands, in a fresh process,
+    with numpy's BLAS on every core the process may use."""
+    cores = _threads_note()
     code = ORACLE_SNIPPET.format(root=ROOT, name=name, budget=budget_s)
-    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
                          timeout=900)
     if res.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        return {"value": None, "unit": "GB/s", "cores": cores, "kind": "oracle",
                 "sample": "failed: " + res.stderr.strip().splitlines()[-1][:200]}
     r = json.loads(res.stdout.strip().splitlines()[-1])
-    return {"value": r["kv_bytes"] / r["median_s"] / 1e9, "unit": "GB/s", "cores": 1,
+    return {"value": r["kv_bytes"] / r["median_s"] / 1e9, "unit": "GB/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"whole {name} step (all 16 sequences x 4 kv heads), float64 numpy, "
-                      f"1 BLAS thread, median of {r['runs']} runs, {r['median_s']:.2f} s/step"}
+            "sample": f"whole {name} step (every sequence and kv head), float64 numpy, "
+                      f"default BLAS threads on {cores} cores ({cpu_model()}), "
+                      f"median of {r['runs']} runs, {r['median_s']:.2f} s/step"}
 
 
 # --------------------------------------------------------------------------
@@ -254,7 +278,8 @@ def run_gpu(args, world, rank, local, dist):
     pools.append((k0, v0))
     for _ in range(args.pools - 1):
         pools.append((k0.clone(), v0.clone()))
-    shape = xqa.make_shape(q, k0, bt, merge_mode=args.merge_mode, kv_dtype=args.kv_dtype,
+    shape = xqa.make_shape(q, k0, bt, min_pages_per_cta=args.min_pages,
+                           merge_mode=args.merge_mode, kv_dtype=args.kv_dtype,
                            kv_layout=args.kv_layout)
     ws = xqa.alloc_workspace(shape, dev)
     out = torch.empty_like(q)
@@ -319,12 +344,21 @@ def run_gpu(args, world, rank, local, dist):
     if sampler is not None:
         time.sleep(0.3)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the timed region is cut into REPEATS consecutive chunks of graph replays
+    # (events between chunks, on the same stream, no synchronisation) for the
+    # spread of the per-step time
+    n_chunks = min(REPEATS, nrep)
+    bounds = [round(i * nrep / n_chunks) for i in range(n_chunks + 1)] if n_chunks else [0]
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(max(0, n_chunks - 1))]
     torch.cuda.synchronize()
     barrier(dist)
     with torch.cuda.stream(stream):  # graph replays launch on the current stream
         t0.record(stream)
-        for _ in range(nrep):
-            g_main.replay()
+        for c in range(max(1, n_chunks)):
+            for _ in range(bounds[c + 1] - bounds[c] if n_chunks else nrep):
+                g_main.replay()
+            if c < len(marks):
+                marks[c].record(stream)
         if g_tail is not None:
             g_tail.replay()
         t1.record(stream)
@@ -333,6 +367,14 @@ def run_gpu(args, world, rank, local, dist):
     barrier(dist)
     clocks = sampler.stop() if sampler is not None else None
     ms_total = t0.elapsed_time(t1)
+    repeats = None
+    if n_chunks >= 2 and g_tail is None:
+        edges = [t0] + marks + [t1]
+        per_step_us = sorted(edges[c].elapsed_time(edges[c + 1]) * 1e3 / ((bounds[c + 1] - bounds[c]) * C)
+                             for c in range(n_chunks))
+        repeats = {"n": n_chunks, "steps_each": (nrep // n_chunks) * C,
+                   "median_us": per_step_us[len(per_step_us) // 2],
+                   "p10_us": _quantile(per_step_us, 0.1), "p90_us": _quantile(per_step_us, 0.9)}
     ms_total_max = reduce_max(dist, ms_total)
     ms_per_step = ms_total_max / args.steps
 
@@ -426,6 +468,7 @@ def run_gpu(args, world, rank, local, dist):
                   f"{2 * w.k_cache.nbytes / 1e6:.0f} MB",
             "timing": f"CUDA graph replays of {C} steps on one stream, CUDA events",
             "merge_mode": shape.merge_mode,
+            "min_pages_per_cta": shape.min_pages_per_cta,
             "kv_dtype": args.kv_dtype,
             "kv_layout": args.kv_layout,
             "q_len": args.q_len,
@@ -445,6 +488,7 @@ def run_gpu(args, world, rank, local, dist):
             "avg_launch_us": part_avg_ms * 1e3,
             "launch_timing": timing_note,
         },
+        "repeats": repeats,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": e2e,
@@ -512,6 +556,14 @@ def run_reference(args, world, rank):
     }
 
 
+def _quantile(sorted_vals, q):
+    """Linear-interpolated quantile of an ascending list."""
+    x = q * (len(sorted_vals) - 1)
+    i = int(x)
+    j = min(i + 1, len(sorted_vals) - 1)
+    return sorted_vals[i] + (sorted_vals[j] - sorted_vals[i]) * (x - i)
+
+
 def _threads_note():
     try:
         return int(os.environ.get("OMP_NUM_THREADS") or 0) or len(os.sched_getaffinity(0))
@@ -549,6 +601,8 @@ def main(argv=None):
     ap.add_argument("--kv-dtype", choices=("e5m2", "e4m3"), default="e5m2")
     ap.add_argument("--kv-layout", choices=("hnd", "nhd"), default="hnd")
     ap.add_argument("--q-len", type=int, default=1, help="new tokens per sequence")
+    ap.add_argument("--min-pages", type=int, default=0,
+                    help="minimum pages per CTA of the split rule (0: the library default)")
     ap.add_argument("--merge-mode", type=int, choices=(0, 1), default=0,
                     help="0: split segments merged inside the partial kernel; 1: combine kernel")
     ap.add_argument("--warm-seconds", type=float, default=1.0)

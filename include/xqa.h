@@ -73,7 +73,7 @@ typedef struct xqa_shape {
   int32_t num_blocks;         /* NB: pages in the K (and V) pool */
   float sm_scale;             /* softmax scale; <= 0 selects 1/sqrt(D) */
   int32_t max_ctas;           /* upper bound on split-KV CTAs; 0 = SM count */
-  int32_t min_pages_per_cta;  /* planner lower bound on pages per CTA; 0 = 8 */
+  int32_t min_pages_per_cta;  /* planner lower bound on pages per CTA; 0 = 16 */
   int32_t merge_mode;         /* how segments split over several CTAs are merged:
                                  0 = by the last CTA to finish one (inside the
                                  partial kernel, default); 1 = by the separate
@@ -182,9 +182,14 @@ xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void
  *   header[4]          = {status, num_ctas, total_pages, num_segments}
  *   seg_start[B*Hkv+1] = exclusive prefix sum of pages per (sequence, kv head)
  *   seg_bad[B*Hkv]     = 1 where the segment's context length is invalid or a
- *                        bad block id was met, else 0 (may be NULL) */
+ *                        bad block id was met, else 0 (may be NULL)
+ *   seg_cost[B*Hkv]    = inclusive prefix sum of the segments' switch costs on
+ *                        the cost line the CTAs are cut on: 0 for an empty
+ *                        segment, 32 page units for one of fewer than 8 pages,
+ *                        else 12 (may be NULL) */
 xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int32_t* header,
-                           int32_t* seg_start, int32_t* seg_bad, void* stream);
+                           int32_t* seg_start, int32_t* seg_bad, int32_t* seg_cost,
+                           void* stream);
 
 /* Size of the device array behind xqa_decode_static_workspace (per device). */
 #define XQA_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)

@@ -15,9 +15,18 @@ this build adopts (a reading) sizes every split from the total work:
   their page counts and ``P = seg_start[-1]`` is the total;
 * the number of CTAs is ``n = 0`` if ``P == 0`` else
   ``min(max_ctas, max(1, ceil(P / min_pages_per_cta)))``;
-* CTA ``i`` owns the flattened pages ``[floor(i*P/n), floor((i+1)*P/n))``, so
-  shares differ by at most one page whatever the length mix: long sequences are
-  split across CTAs, short ones share a CTA;
+* the work is cut on a *cost line*: the segments are laid end to end, each
+  preceded by its switch cost ``seg_cost(pages)`` (0 for an empty segment,
+  32 for fewer than 8 pages, else 12, in page units: the measured time of a
+  segment switch inside a CTA of the GPU kernel, which the pages do not
+  state; with these costs a CTA holding many tiny segments no longer takes
+  several times longer than the rest); page ``p`` of segment ``s`` sits
+  at position ``p + cc[s]`` with ``cc[s]`` the sum of the costs of segments
+  ``0..s``, and the line is ``V = P + cc[-1]`` long;
+* CTA ``i`` owns the positions ``[floor(i*V/n), floor((i+1)*V/n))`` and so
+  the pages there, a contiguous run (possibly empty): every CTA gets the same
+  cost whatever the length mix, long sequences are split across CTAs, short
+  ones share a CTA and many tiny ones are spread over several;
 * the intersection of CTA ``i`` with segment ``s`` is a *piece*; its partial
   result slot is ``i + s`` (unique, since walking the flattened order every
   piece boundary advances ``i`` or ``s``).
@@ -47,6 +56,42 @@ def segment_starts(pages) -> np.ndarray:
     return out
 
 
+SEG_COST_BIG = 12
+SEG_COST_SMALL = 32
+SMALL_SEG_PAGES = 8
+
+
+def seg_cost(pages) -> np.ndarray:
+    """Switch cost of each segment on the cost line, in page units."""
+    pages = np.asarray(pages, dtype=np.int64)
+    return np.where(pages <= 0, 0, np.where(pages < SMALL_SEG_PAGES, SEG_COST_SMALL, SEG_COST_BIG))
+
+
+def cost_prefix(seg_start) -> np.ndarray:
+    """cc[s] = cost of segments 0..s (inclusive): int64 [nseg]."""
+    return np.cumsum(seg_cost(np.diff(np.asarray(seg_start, dtype=np.int64)))).astype(np.int64)
+
+
+def line_length(seg_start, cc) -> int:
+    return int(seg_start[-1]) + (int(cc[-1]) if len(cc) else 0)
+
+
+def page_position(p: int, seg_start, cc) -> int:
+    """Position of flattened page p on the cost line."""
+    s = int(np.searchsorted(seg_start, p, side="right") - 1)
+    return int(p) + int(cc[s])
+
+
+def page_at(a: int, seg_start, cc) -> int:
+    """The first page at a position >= a (P if there is none)."""
+    seg_start = np.asarray(seg_start, dtype=np.int64)
+    for s in range(len(cc)):
+        first, end = int(seg_start[s]) + int(cc[s]), int(seg_start[s + 1]) + int(cc[s])
+        if end > a:
+            return int(seg_start[s]) if a <= first else int(seg_start[s]) + (a - first)
+    return int(seg_start[-1])
+
+
 def num_ctas(total_pages: int, max_ctas: int, min_pages_per_cta: int) -> int:
     if total_pages <= 0:
         return 0
@@ -54,23 +99,24 @@ def num_ctas(total_pages: int, max_ctas: int, min_pages_per_cta: int) -> int:
     return int(min(int(max_ctas), max(1, want)))
 
 
-def cta_range(i: int, total_pages: int, n: int):
-    """Flattened page range [begin, end) of CTA ``i``."""
-    return (i * total_pages) // n, ((i + 1) * total_pages) // n
+def cta_range(i: int, seg_start, cc, n: int):
+    """Flattened page range [begin, end) of CTA ``i``: its positions on the line."""
+    line = line_length(seg_start, cc)
+    return page_at((i * line) // n, seg_start, cc), page_at(((i + 1) * line) // n, seg_start, cc)
 
 
-def cta_of_page(p: int, total_pages: int, n: int) -> int:
-    """The CTA whose range holds flattened page ``p`` (closed form)."""
-    return ((p + 1) * n - 1) // total_pages
+def cta_of_page(p: int, seg_start, cc, n: int) -> int:
+    """The CTA whose range holds flattened page ``p`` (closed form on its position)."""
+    return ((page_position(p, seg_start, cc) + 1) * n - 1) // line_length(seg_start, cc)
 
 
 def pieces(seg_start, n: int):
     """All (cta, segment, page_begin, page_end, slot) pieces, in flattened order."""
     seg_start = np.asarray(seg_start, dtype=np.int64)
-    total = int(seg_start[-1])
+    cc = cost_prefix(seg_start)
     out = []
     for i in range(n):
-        a, e = cta_range(i, total, n)
+        a, e = cta_range(i, seg_start, cc, n)
         if a == e:
             continue
         s = int(np.searchsorted(seg_start, a, side="right") - 1)
@@ -95,6 +141,7 @@ def plan(context_lens, num_kv_heads: int, max_blocks_per_seq: int, max_ctas: int
     n = num_ctas(total, max_ctas, min_pages_per_cta)
     return {
         "seg_start": starts,
+        "seg_cc": cost_prefix(starts),
         "seg_bad": bad,
         "total_pages": total,
         "num_ctas": n,

@@ -93,7 +93,7 @@ _SIGS = {
     "xqa_combine": [_P, _F, _P, _SHAPE, _P, _SZ, _P],
     "xqa_dequant_e5m2": [_P, _SZ, _F, _P, _P, _P],
     "xqa_read_status": [_P, ctypes.POINTER(ctypes.c_int32), _P],
-    "xqa_read_plan": [_P, _SHAPE, _P, _P, _P, _P],
+    "xqa_read_plan": [_P, _SHAPE, _P, _P, _P, _P, _P],
     "xqa_status_string": [ctypes.c_int],
     "xqa_decode_static_workspace": [_P, _P, _P, _P, _P, _F, _F, _P, _SHAPE, _P],
     "xqa_decode_device_scales": [_P, _P, _P, _P, _P, _P, _P, _P, _SHAPE, _P, _SZ, _P],
@@ -279,12 +279,15 @@ def xqa_read_plan(workspace: torch.Tensor, shape: XqaShape, stream=None) -> dict
     header = np.zeros(4, np.int32)
     seg_start = np.zeros(nseg + 1, np.int32)
     seg_bad = np.zeros(nseg, np.int32)
+    seg_cost = np.zeros(nseg, np.int32)
     _check(load_library().xqa_read_plan(_cuda(workspace, torch.uint8, "workspace"),
                                         ctypes.byref(shape), header.ctypes.data,
                                         seg_start.ctypes.data, seg_bad.ctypes.data,
-                                        _stream_handle(stream)), "xqa_read_plan")
+                                        seg_cost.ctypes.data, _stream_handle(stream)),
+           "xqa_read_plan")
     return {"status": int(header[0]), "num_ctas": int(header[1]), "total_pages": int(header[2]),
-            "num_segments": int(header[3]), "seg_start": seg_start, "seg_bad": seg_bad}
+            "num_segments": int(header[3]), "seg_start": seg_start, "seg_bad": seg_bad,
+            "seg_cc": seg_cost}
 
 
 def xqa_decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens, k_scale: float,

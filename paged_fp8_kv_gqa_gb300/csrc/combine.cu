@@ -47,31 +47,53 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
       store_half4(o, v, v, v, v);
       continue;
     }
-    const int ilo = (int)(((long long)(sb + 1) * n - 1) / total);
-    const int ihi = (int)(((long long)se * n - 1) / total);
+    // the CTAs holding the first and the last page, on the planner's cost line
+    const long long line = total + p.seg_cc[p.header[3] - 1];
+    const int ilo = cta_of_vpos((long long)sb + p.seg_cc[s], line, n);
+    const int ihi = cta_of_vpos((long long)se - 1 + p.seg_cc[s], line, n);
     if (ilo == ihi) continue;  // written whole by its partial CTA
     if (bad) {
       const float v = __int_as_float(0x7fc00000);
       store_half4(o, v, v, v, v);
       continue;
     }
+    // the maxima 16 pieces at a time, then the weighted sums 8 at a time (every
+    // load of a batch issued before any is used; the sums in piece order)
     float M = -INFINITY;
-    for (int i = ilo; i <= ihi; ++i) {
-      const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
-      M = fmaxf(M, slot[kSlotM + col]);
+    for (int base = ilo; base <= ihi; base += 16) {
+      float mb[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (base + k <= ihi) mb[k] = p.partials[(size_t)(base + k + s) * kSlotFloats + kSlotM + col];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (base + k <= ihi) M = fmaxf(M, mb[k]);
     }
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = ilo; i <= ihi; ++i) {
-      const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
-      const float mi = slot[kSlotM + col];
-      const float w = (mi == -INFINITY) ? 0.f : ex2(mi - M);
-      L += w * slot[kSlotL + col];
-      const float4 v = *reinterpret_cast<const float4*>(slot + col * kHeadDim + dq);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+    for (int base = ilo; base <= ihi; base += 8) {
+      float mb[8], lb[8];
+      float4 vb[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (base + k <= ihi) {
+          const float* slot = p.partials + (size_t)(base + k + s) * kSlotFloats;
+          mb[k] = slot[kSlotM + col];
+          lb[k] = slot[kSlotL + col];
+          vb[k] = *reinterpret_cast<const float4*>(slot + col * kHeadDim + dq);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (base + k <= ihi) {
+          const float w = (mb[k] == -INFINITY) ? 0.f : ex2(mb[k] - M);
+          L += w * lb[k];
+          acc.x += w * vb[k].x;
+          acc.y += w * vb[k].y;
+          acc.z += w * vb[k].z;
+          acc.w += w * vb[k].w;
+        }
+      }
     }
     const float r = (L > 0.f) ? v_scale / L : 0.f;  // a new token with no visible token: 0
     store_half4(o, acc.x * r, acc.y * r, acc.z * r, acc.w * r);

@@ -332,10 +332,12 @@ __device__ __forceinline__ void store_half4(__half* o, float a, float b, float c
 // and the last of its range) into fp16 rows, thread: column col, dims
 // dq..dq+3. Pieces were written by other CTAs: read through L2. The bad flags
 // and, for segments of at most kFew pieces, every piece of both segments are
-// loaded before any is used (one round trip for the whole merge).
+// loaded before any is used (one round trip for the whole merge); a segment of
+// more pieces takes its maxima 16 and its weighted sums 8 pieces per round trip.
 __device__ __forceinline__ void merge_segments(const PartialParams& p, const int (&ms)[2], int nm,
-                                               const int32_t* segs, int total, int n, int col,
-                                               int dq, float v_scale) {
+                                               const int32_t* segs, const int32_t* cc,
+                                               long long line, int n, int col, int dq,
+                                               float v_scale) {
   if (col >= p.group * p.q_len) return;
   constexpr int kFew = 4;
   int ilo[2], ihi[2], bad[2];
@@ -345,8 +347,8 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
   for (int j = 0; j < 2; ++j) {
     if (j < nm) {
       const int s = ms[j];
-      ilo[j] = cta_of_page(segs[s], total, n);
-      ihi[j] = cta_of_page(segs[s + 1] - 1, total, n);
+      ilo[j] = cta_of_vpos((long long)segs[s] + cc[s], line, n);
+      ihi[j] = cta_of_vpos((long long)segs[s + 1] - 1 + cc[s], line, n);
       bad[j] = __ldcg(&p.seg_bad[s]);
 #pragma unroll
       for (int k = 0; k < kFew; ++k) {
@@ -387,19 +389,40 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
           acc.w += w * oi[j][k].w;
         }
       }
-    } else {  // many pieces (small shares): two passes through L2
-      for (int i = ilo[j]; i <= ihi[j]; ++i)
-        M = fmaxf(M, __ldcg(p.partials + (size_t)(i + s) * kSlotFloats + kSlotM + col));
-      for (int i = ilo[j]; i <= ihi[j]; ++i) {
-        const float* slot = p.partials + (size_t)(i + s) * kSlotFloats;
-        const float m = __ldcg(slot + kSlotM + col);
-        const float w = (m == -INFINITY) ? 0.f : ex2(m - M);
-        L += w * __ldcg(slot + kSlotL + col);
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
-        acc.x += w * x.x;
-        acc.y += w * x.y;
-        acc.z += w * x.z;
-        acc.w += w * x.w;
+    } else {  // many pieces: the maxima 16 at a time, then the sums 8 at a time
+      for (int base = ilo[j]; base <= ihi[j]; base += 16) {
+        float mb[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (base + k <= ihi[j])
+            mb[k] = __ldcg(p.partials + (size_t)(base + k + s) * kSlotFloats + kSlotM + col);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (base + k <= ihi[j]) M = fmaxf(M, mb[k]);
+      }
+      for (int base = ilo[j]; base <= ihi[j]; base += 8) {
+        float mb[8], lb[8];
+        float4 ob[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + k <= ihi[j]) {
+            const float* slot = p.partials + (size_t)(base + k + s) * kSlotFloats;
+            mb[k] = __ldcg(slot + kSlotM + col);
+            lb[k] = __ldcg(slot + kSlotL + col);
+            ob[k] = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + k <= ihi[j]) {
+            const float w = (mb[k] == -INFINITY) ? 0.f : ex2(mb[k] - M);
+            L += w * lb[k];
+            acc.x += w * ob[k].x;
+            acc.y += w * ob[k].y;
+            acc.z += w * ob[k].z;
+            acc.w += w * ob[k].w;
+          }
+        }
       }
     }
     const float rr = (L > 0.f) ? v_scale / L : 0.f;  // a new token with no visible token: 0
@@ -423,8 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int stage_bad[kStages];
   __shared__ int abort_flag;
 
-  __shared__ int scan_warp[kWarps];
-  __shared__ int scan_carry;
+  __shared__ int scan_warp[kWarps], scan_warp_cost[kWarps];
+  __shared__ int scan_carry, scan_carry_cost;
+  __shared__ long long cost_line;  // kept here: the end of the kernel reads it back
+  __shared__ int range_lo, range_hi, range_seg;  // this CTA's pages, first segment
   // split pieces of this CTA (at most its first and last segment), whose
   // merge tickets are taken once the whole range is done
   __shared__ int pend_seg[2], pend_poison[2], pend_last[2];
@@ -448,14 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* merge_bufs = reinterpret_cast<float*>(stages + kStages * kStageBytes);
   int32_t* seg_cache = reinterpret_cast<int32_t*>(merge_bufs + kBufs * Geom::kMergeBufFloats);
   int32_t* ctx_cache = seg_cache + kSegCache;  // context length per sequence
+  int32_t* cc_cache = ctx_cache + kSegCache;   // cost-line prefix per segment
 
   // ---- the plan: computed here when the segment table fits in shared memory
   // (same integer rule as the planner kernel), else read from the planner ----
   const bool segs_in_smem = nseg + 1 <= kSegCache;
   const int32_t* segs;
+  const int32_t* cc;
   int total, n;
   if (segs_in_smem) {
-    if (tid == 0) scan_carry = 0;
+    if (tid == 0) scan_carry = scan_carry_cost = 0;
     __syncthreads();
     const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
     for (int base = 0; base < p.batch; base += kThreads) {
@@ -466,33 +493,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctx_cache[b] = ctx;
         pages = (ctx < 0 || (long long)ctx > max_ctx) ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
       }
-      int incl = pages;
+      const int cost = seg_cost(pages);  // every kv head's segment of sequence b
+      int incl = pages, incl_cost = cost;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int u = __shfl_up_sync(kFull, incl, off);
-        if (lane >= off) incl += u;
+        const int uc = __shfl_up_sync(kFull, incl_cost, off);
+        if (lane >= off) {
+          incl += u;
+          incl_cost += uc;
+        }
       }
-      if (lane == 31) scan_warp[warp] = incl;
+      if (lane == 31) {
+        scan_warp[warp] = incl;
+        scan_warp_cost[warp] = incl_cost;
+      }
       __syncthreads();
-      int before = scan_carry;
-      for (int w = 0; w < warp; ++w) before += scan_warp[w];
+      int before = scan_carry, before_cost = scan_carry_cost;
+      for (int w = 0; w < warp; ++w) {
+        before += scan_warp[w];
+        before_cost += scan_warp_cost[w];
+      }
       const int excl = before + incl - pages;
+      const int excl_cost = before_cost + incl_cost - cost;
       if (b < p.batch)
-        for (int h = 0; h < p.num_kv_heads; ++h)
+        for (int h = 0; h < p.num_kv_heads; ++h) {
           seg_cache[b * p.num_kv_heads + h] = excl * p.num_kv_heads + h * pages;
+          cc_cache[b * p.num_kv_heads + h] = excl_cost * p.num_kv_heads + (h + 1) * cost;
+        }
       __syncthreads();
-      if (tid == kThreads - 1) scan_carry = excl + pages;
+      if (tid == kThreads - 1) {
+        scan_carry = excl + pages;
+        scan_carry_cost = excl_cost + cost;
+      }
       __syncthreads();
     }
     total = scan_carry * p.num_kv_heads;
     if (tid == 0) seg_cache[nseg] = total;
     n = num_ctas_for(total, p.n_max, p.min_pages);
     segs = seg_cache;
+    cc = cc_cache;
   } else {
     griddep_wait();
     total = p.header[2];
     n = p.header[1];
     segs = p.seg_start;
+    cc = p.seg_cc;
   }
   __syncthreads();
 
@@ -513,11 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (cta >= n) return;
-  const int cbeg = (int)(((long long)cta * total) / n);
-  const int cend = (int)(((long long)(cta + 1) * total) / n);
-  const int npages = cend - cbeg;
-
+  // This CTA's positions [vlo, vhi) on the cost line, and the pages there: the
+  // first page at a position >= a lies in the first segment whose pages end
+  // past a. One parallel pass over the segments finds both ends (and the
+  // first segment) in shared memory, in place of two dependent searches.
+  const long long line = (long long)total + (nseg > 0 ? cc[nseg - 1] : 0);
+  const long long vlo = ((long long)cta * line) / n, vhi = ((long long)(cta + 1) * line) / n;
   if (tid == 0) {
+    cost_line = line;
+    range_lo = range_hi = total;  // no segment ends past the position
+    range_seg = nseg;
     for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -525,7 +576,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_v);
   }
   __syncthreads();
-  const int s_first = find_segment(segs, 0, nseg, cbeg);
+  for (int s = tid; s < nseg; s += kThreads) {
+    const long long end = (long long)segs[s + 1] + cc[s];                 // past its last page
+    const long long prev = s > 0 ? (long long)segs[s] + cc[s - 1] : -1;  // previous one's end
+    const long long first = (long long)segs[s] + cc[s];                   // its first page
+    if (end > vlo && prev <= vlo) {
+      range_lo = vlo <= first ? segs[s] : (int)(segs[s] + (vlo - first));
+      range_seg = s;
+    }
+    if (end > vhi && prev <= vhi) range_hi = vhi <= first ? segs[s] : (int)(segs[s] + (vhi - first));
+  }
+  __syncthreads();
+  const int cbeg = range_lo, cend = range_hi;
+  const int npages = cend - cbeg;
+  if (npages <= 0) return;  // its share of the line is segment switch cost only
+  const int s_first = range_seg;
   volatile int* abort = &abort_flag;
   const uint64_t policy = l2_evict_first_policy();
   const int g = lane >> 2, c = lane & 3;
@@ -775,6 +840,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The CTA whose ticket completes a segment merges all its pieces in slot
   // order, exactly as the combine kernel would.
   if (npend > 0) {
+    // the cost line again, read back rather than kept live through the loop
+    const int32_t* cc = segs_in_smem ? cc_cache : p.seg_cc;
+    const long long line = *reinterpret_cast<volatile long long*>(&cost_line);
     griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
     consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
     if (tid < npend) {
@@ -782,7 +850,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pend_poison[tid]) atomicOr(&p.seg_bad[ps], 1);
       int last = 0;
       if (p.fused_merge) {
-        const int ilo = cta_of_page(segs[ps], total, n), ihi = cta_of_page(segs[ps + 1] - 1, total, n);
+        const int ilo = cta_of_vpos((long long)segs[ps] + cc[ps], line, n);
+        const int ihi = cta_of_vpos((long long)segs[ps + 1] - 1 + cc[ps], line, n);
         // release: this CTA's slots (ordered before by the barrier) are visible
         // to whoever takes a later ticket; acquire: the earlier pieces are
         // visible to this CTA after the next barrier
@@ -801,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ms[2] = {m0, m1};
     if (nm > 0)
       for (int col = tid >> 5; col < kCols; col += kWarps)
-        merge_segments(p, ms, nm, segs, total, n, col, (tid & 31) * 4, v_scale);
+        merge_segments(p, ms, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
   }
 
   // Drain: after an abort some issued copies may not have been waited for; every

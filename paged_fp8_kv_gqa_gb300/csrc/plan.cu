@@ -2,10 +2,13 @@
 //
 // Reads context_lens[B] and publishes, in the workspace, the pages of every
 // (sequence, kv head) segment as an exclusive prefix sum, the bad-segment
-// flags, the total page count and the number of partial-kernel CTAs. CTA i of
-// the partial kernel then owns flattened pages [floor(i*P/n), floor((i+1)*P/n)):
-// every CTA gets the same share whatever the length mix, long sequences are
-// split across CTAs and short ones share a CTA. This answers the two failure
+// flags, the cost-line prefix, the total page count and the number of
+// partial-kernel CTAs. The cost line lays the segments end to end, each
+// preceded by its switch cost (seg_cost: 12 page units, 32 for a segment of
+// fewer than 8 pages); CTA i of the partial kernel owns the pages at positions
+// [floor(i*V/n), floor((i+1)*V/n)) of that line. Every CTA gets the same cost
+// whatever the length mix: long sequences are split across CTAs, short ones
+// share a CTA, and many tiny segments are spread over several. This answers the two failure
 // modes recorded on the page "[Kernel][WIP] Follow up FlashNext batch HC fusion
 // and QSA route audit" (section "Test Result"): a capacity-sized grid with
 // empty CTAs on short contexts, and fixed grids that regress long ones. The
@@ -38,16 +41,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   griddep_wait();               // everything earlier on the stream is complete
   griddep_launch_dependents();  // the partial kernel may start its prologue now
   const int nseg = batch * num_kv_heads;
+  const WsLayout lay = ws_layout(nseg, 0);
   int32_t* header = ws;
-  int32_t* seg_start = ws + 4;
-  int32_t* seg_bad = seg_start + nseg + 1;
-  int32_t* seg_count = seg_bad + nseg;
-  __shared__ int warp_total[kPlanThreads / 32];
-  __shared__ int carry;
+  int32_t* seg_start = ws + lay.seg_start_off / 4;
+  int32_t* seg_bad = ws + lay.seg_bad_off / 4;
+  int32_t* seg_count = ws + lay.seg_count_off / 4;
+  int32_t* seg_cc = ws + lay.seg_cc_off / 4;
+  __shared__ int warp_total[kPlanThreads / 32], warp_cost[kPlanThreads / 32];
+  __shared__ int carry, carry_cost;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     header[0] = XQA_OK;
     carry = 0;
+    carry_cost = 0;
   }
   __syncthreads();
   const long long max_ctx = (long long)max_blocks_per_seq * kBlockSize;
@@ -62,19 +68,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       seg_bad[s] = bad ? 1 : 0;
       seg_count[s] = 0;
     }
+    const int cost = seg_cost(pages);
     const int incl = warp_inclusive_scan(pages);
-    if (lane == 31) warp_total[warp] = incl;
+    const int incl_cost = warp_inclusive_scan(cost);
+    if (lane == 31) {
+      warp_total[warp] = incl;
+      warp_cost[warp] = incl_cost;
+    }
     __syncthreads();
     if (warp == 0) {
       constexpr int kPlanWarps = kPlanThreads / 32;
       const int t = warp_inclusive_scan(lane < kPlanWarps ? warp_total[lane] : 0);
-      if (lane < kPlanWarps) warp_total[lane] = t;
+      const int tc = warp_inclusive_scan(lane < kPlanWarps ? warp_cost[lane] : 0);
+      if (lane < kPlanWarps) {
+        warp_total[lane] = t;
+        warp_cost[lane] = tc;
+      }
     }
     __syncthreads();
     const int excl = carry + incl - pages + (warp > 0 ? warp_total[warp - 1] : 0);
-    if (s < nseg) seg_start[s] = excl;
+    const int cc = carry_cost + incl_cost + (warp > 0 ? warp_cost[warp - 1] : 0);
+    if (s < nseg) {
+      seg_start[s] = excl;
+      seg_cc[s] = cc;
+    }
     __syncthreads();
-    if (tid == kPlanThreads - 1) carry = excl + pages;
+    if (tid == kPlanThreads - 1) {
+      carry = excl + pages;
+      carry_cost = cc;
+    }
     __syncthreads();
   }
   if (tid == 0) {

@@ -197,6 +197,7 @@ xqa_status_t attend_partial_impl(const void* q, const uint8_t* k_cache, const ui
   p.seg_start = reinterpret_cast<const int32_t*>(base + r.ws.seg_start_off);
   p.seg_bad = reinterpret_cast<int32_t*>(base + r.ws.seg_bad_off);
   p.seg_count = reinterpret_cast<int32_t*>(base + r.ws.seg_count_off);
+  p.seg_cc = reinterpret_cast<const int32_t*>(base + r.ws.seg_cc_off);
   p.partials = reinterpret_cast<float*>(base + r.ws.partials_off);
   p.n_max = r.n_max;
   p.min_pages = r.min_pages;
@@ -235,6 +236,7 @@ xqa_status_t combine_impl(const int32_t* context_lens, float v_scale, const floa
   p.header = ws_i32(workspace);
   p.seg_start = reinterpret_cast<const int32_t*>(base + r.ws.seg_start_off);
   p.seg_bad = reinterpret_cast<const int32_t*>(base + r.ws.seg_bad_off);
+  p.seg_cc = reinterpret_cast<const int32_t*>(base + r.ws.seg_cc_off);
   p.partials = reinterpret_cast<const float*>(base + r.ws.partials_off);
   p.num_q_heads = r.hq;
   p.num_kv_heads = r.hkv;
@@ -347,7 +349,8 @@ xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void
 }
 
 xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int32_t* header,
-                           int32_t* seg_start, int32_t* seg_bad, void* stream) {
+                           int32_t* seg_start, int32_t* seg_bad, int32_t* seg_cost,
+                           void* stream) {
   if (!workspace || !header || !seg_start) return XQA_ERR_NULL;
   Resolved r;
   xqa_status_t st = resolve(shape, &r);
@@ -361,6 +364,9 @@ xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int3
     return XQA_ERR_LAUNCH;
   if (seg_bad && cudaMemcpyAsync(seg_bad, base + r.ws.seg_bad_off, (size_t)r.nseg * 4,
                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return XQA_ERR_LAUNCH;
+  if (seg_cost && cudaMemcpyAsync(seg_cost, base + r.ws.seg_cc_off, (size_t)r.nseg * 4,
+                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return XQA_ERR_LAUNCH;
   if (cudaStreamSynchronize(s) != cudaSuccess) return XQA_ERR_LAUNCH;
   return XQA_OK;

@@ -39,10 +39,18 @@ struct PartialGeom {
   static constexpr int kMergeBufs = NT == 1 ? 2 : 1;
   static constexpr int kSmem = 1024 /* alignment slack for the 1024-B swizzle atom */ +
                                kStages * kStageBytes + kMergeBufs * kMergeBufFloats * 4 +
-                               kSegCache * 4 /* segment starts */ + kSegCache * 4 /* lengths */;
+                               kSegCache * 4 /* segment starts */ + kSegCache * 4 /* lengths */ +
+                               kSegCache * 4 /* cost prefix */;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
-constexpr int kDefaultMinPagesPerCta = 8;
+constexpr int kDefaultMinPagesPerCta = 16;
+// Split rule cost line: every non-empty segment costs seg_cost(pages) page
+// units on top of its pages (the measured time of a segment switch inside a
+// CTA: about 12 pages' worth of streaming; a segment of fewer than 8 pages also
+// leaves most warps idle and costs about 32).
+constexpr int kSegCostBig = 12;
+constexpr int kSegCostSmall = 32;
+constexpr int kSmallSegPages = 8;
 constexpr int kPlanThreads = 256;  // small enough to share an SM with a partial CTA
 constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
 
@@ -63,6 +71,7 @@ struct WsLayout {
   size_t seg_start_off;  // int32 [nseg + 1]
   size_t seg_bad_off;    // int32 [nseg]
   size_t seg_count_off;  // int32 [nseg]: pieces finished, for the in-kernel merge
+  size_t seg_cc_off;     // int32 [nseg]: cost of segments 0..s (inclusive), see seg_cost
   size_t partials_off;   // float [(n_max + nseg) * kSlotFloats]
   size_t total;
 };
@@ -72,7 +81,8 @@ __host__ __device__ inline WsLayout ws_layout(long long nseg, long long n_max) {
   l.seg_start_off = 16;
   l.seg_bad_off = l.seg_start_off + 4 * (size_t)(nseg + 1);
   l.seg_count_off = l.seg_bad_off + 4 * (size_t)nseg;
-  size_t end = l.seg_count_off + 4 * (size_t)nseg;
+  l.seg_cc_off = l.seg_count_off + 4 * (size_t)nseg;
+  size_t end = l.seg_cc_off + 4 * (size_t)nseg;
   l.partials_off = (end + 255) & ~(size_t)255;
   l.total = l.partials_off + (size_t)(n_max + nseg) * kSlotFloats * sizeof(float);
   return l;
@@ -256,6 +266,35 @@ __host__ __device__ inline int num_ctas_for(int total_pages, int n_max, int min_
 // CTA owning flattened page p when P pages are split over n CTAs.
 __host__ __device__ inline int cta_of_page(long long page, long long total, long long n) {
   return (int)(((page + 1) * n - 1) / total);
+}
+
+// The cost line. Segment s (pages segs[s] .. segs[s+1]) costs
+// seg_cost(pages) units before its pages; cc[s] = sum of the costs of
+// segments 0..s. Page p of segment s sits at position p + cc[s], the line is
+// V = P + cc[nseg - 1] long, CTA i takes the positions [floor(iV/n),
+// floor((i+1)V/n)) and so a contiguous (possibly empty) run of pages.
+__host__ __device__ inline int seg_cost(int pages) {
+  return pages <= 0 ? 0 : (pages < kSmallSegPages ? kSegCostSmall : kSegCostBig);
+}
+
+// CTA owning position v of a line of length V split over n CTAs.
+__host__ __device__ inline int cta_of_vpos(long long v, long long line, long long n) {
+  return (int)(((v + 1) * n - 1) / line);
+}
+
+// The first page at a position >= a (P when there is none): the first
+// segment whose pages end past a on the line, then the offset into it.
+__host__ __device__ inline int page_of_vpos(const int32_t* segs, const int32_t* cc, int nseg,
+                                            long long a) {
+  int lo = 0, hi = nseg;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((long long)segs[mid + 1] + cc[mid] > a) hi = mid;
+    else lo = mid + 1;
+  }
+  if (lo == nseg) return segs[nseg];
+  const long long first = (long long)segs[lo] + cc[lo];
+  return a <= first ? segs[lo] : (int)(segs[lo] + (a - first));
 }
 
 // Device-scope fetch-and-add with acquire-release ordering.

@@ -16,6 +16,7 @@ struct PartialParams {
   const int32_t* seg_start;  // [nseg + 1]
   int32_t* seg_bad;          // [nseg]
   int32_t* seg_count;        // [nseg] pieces finished (in-kernel merge tickets)
+  const int32_t* seg_cc;     // [nseg] cost-line prefix (planner's; see seg_cost)
   float* partials;           // [(n_max + nseg) * kSlotFloats]
   int batch, num_q_heads, num_kv_heads, group, max_blocks_per_seq, num_blocks;
   int q_len;                 // new tokens per sequence (q, out: [B, q_len, Hq, D])
@@ -33,6 +34,7 @@ struct CombineParams {
   const int32_t* header;
   const int32_t* seg_start;
   const int32_t* seg_bad;
+  const int32_t* seg_cc;
   const float* partials;
   int num_q_heads, num_kv_heads, group, q_len;
   float v_scale;

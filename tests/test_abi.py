@@ -52,7 +52,8 @@ def test_host_validation_without_device(lib):
     n = ctypes.c_size_t(0)
     assert lib.xqa_workspace_size(ctypes.byref(shape), ctypes.byref(n)) == xqa.XQA_OK
     nseg = 64
-    head = 16 + 4 * (nseg + 1) + 4 * nseg + 4 * nseg
+    # header, segment starts, bad flags, piece counters, cost-line prefix
+    head = 16 + 4 * (nseg + 1) + 4 * nseg + 4 * nseg + 4 * nseg
     head = (head + 255) // 256 * 256
     assert n.value == head + (152 + nseg) * (16 * 128 + 32) * 4
     for bad in (

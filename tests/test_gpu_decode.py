@@ -149,9 +149,10 @@ def test_plan_matches_oracle_bit_exactly():
         d.run()
         got = xqa.xqa_read_plan(d.ws, d.shape)
         n_max = max_ctas or torch.cuda.get_device_properties(0).multi_processor_count
-        ref = plan.plan(w.context_lens, hkv, w.max_blocks_per_seq, n_max, minp or 8)
+        ref = plan.plan(w.context_lens, hkv, w.max_blocks_per_seq, n_max, minp or 16)
         assert got["status"] == 0
         assert np.array_equal(got["seg_start"], ref["seg_start"])
+        assert np.array_equal(got["seg_cc"], ref["seg_cc"])
         assert np.array_equal(got["seg_bad"].astype(bool), ref["seg_bad"])
         assert got["num_ctas"] == ref["num_ctas"]
         assert got["total_pages"] == ref["total_pages"]
