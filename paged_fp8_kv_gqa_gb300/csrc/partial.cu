@@ -332,8 +332,11 @@ __device__ __forceinline__ void store_half4(__half* o, float a, float b, float c
 // and the last of its range) into fp16 rows, thread: column col, dims
 // dq..dq+3. Pieces were written by other CTAs: read through L2. The bad flags
 // and, for segments of at most kFew pieces, every piece of both segments are
-// loaded before any is used (one round trip for the whole merge); a segment of
-// more pieces takes its maxima 16 and its weighted sums 8 pieces per round trip.
+// loaded before any is used (one round trip for the whole merge); in one-tile
+// kernels a segment of up to 16 pieces takes one round trip of its own, a
+// longer one two per 16 (two-tile kernels, short of registers: the maxima 16
+// and the sums 8 pieces per round trip).
+template <bool kWide>  // one round trip for up to 16 pieces (else 8, fewer registers)
 __device__ __forceinline__ void merge_segments(const PartialParams& p, const int (&ms)[2], int nm,
                                                const int32_t* segs, const int32_t* cc,
                                                long long line, int n, int col, int dq,
@@ -389,7 +392,34 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
           acc.w += w * oi[j][k].w;
         }
       }
-    } else {  // many pieces: the maxima 16 at a time, then the sums 8 at a time
+    } else if (kWide && ihi[j] - ilo[j] < 16) {  // up to 16 pieces: still one round trip
+      float mb[16], lb[16];
+      float4 ob[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (ilo[j] + k <= ihi[j]) {
+          const float* slot = p.partials + (size_t)(ilo[j] + k + s) * kSlotFloats;
+          mb[k] = __ldcg(slot + kSlotM + col);
+          lb[k] = __ldcg(slot + kSlotL + col);
+          ob[k] = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (ilo[j] + k <= ihi[j]) M = fmaxf(M, mb[k]);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (ilo[j] + k <= ihi[j]) {
+          const float w = (mb[k] == -INFINITY) ? 0.f : ex2(mb[k] - M);
+          L += w * lb[k];
+          acc.x += w * ob[k].x;
+          acc.y += w * ob[k].y;
+          acc.z += w * ob[k].z;
+          acc.w += w * ob[k].w;
+        }
+      }
+    } else {  // more: the maxima 16 per round trip, then the weighted sums
+      constexpr int kSum = kWide ? 16 : 8;  // pieces per round trip of the sums
       for (int base = ilo[j]; base <= ihi[j]; base += 16) {
         float mb[16];
 #pragma unroll
@@ -400,11 +430,11 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
         for (int k = 0; k < 16; ++k)
           if (base + k <= ihi[j]) M = fmaxf(M, mb[k]);
       }
-      for (int base = ilo[j]; base <= ihi[j]; base += 8) {
-        float mb[8], lb[8];
-        float4 ob[8];
+      for (int base = ilo[j]; base <= ihi[j]; base += kSum) {
+        float mb[kSum], lb[kSum];
+        float4 ob[kSum];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kSum; ++k) {
           if (base + k <= ihi[j]) {
             const float* slot = p.partials + (size_t)(base + k + s) * kSlotFloats;
             mb[k] = __ldcg(slot + kSlotM + col);
@@ -413,7 +443,7 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
           }
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kSum; ++k) {
           if (base + k <= ihi[j]) {
             const float w = (mb[k] == -INFINITY) ? 0.f : ex2(mb[k] - M);
             L += w * lb[k];
@@ -870,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ms[2] = {m0, m1};
     if (nm > 0)
       for (int col = tid >> 5; col < kCols; col += kWarps)
-        merge_segments(p, ms, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
+        merge_segments<NT == 1>(p, ms, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
   }
 
   // Drain: after an abort some issued copies may not have been waited for; every
