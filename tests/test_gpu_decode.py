@@ -99,6 +99,19 @@ def test_split_count_does_not_change_the_result(max_ctas, min_pages, merge_mode)
     assert_close(out, oracle_out(name), f"{name} max_ctas={max_ctas}")
 
 
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_ctas_with_only_switch_cost_on_the_line(merge_mode):
+    # tiny segments and one CTA per page: several CTAs' shares of the cost line
+    # fall inside a segment's switch cost and hold no page (they exit early)
+    w = wl.make_custom([16, 1, 15, 16, 40, 3], 4, 2, seed=62)
+    starts = plan.plan(w.context_lens, 2, w.max_blocks_per_seq, 300, 1)
+    n, cc = starts["num_ctas"], starts["seg_cc"]
+    empty = [i for i in range(n) if np.subtract(*plan.cta_range(i, starts["seg_start"], cc, n)) == 0]
+    assert len(empty) > 0
+    out = run(w, max_ctas=300, min_pages=1, merge_mode=merge_mode)
+    assert_close(out, oracle_of(w), "empty cost-line shares")
+
+
 def test_single_token_context_is_the_v_row_bitwise():
     w = wl.make_custom([1, 1, 1], 16, 2, seed=21, k_scale=0.5, v_scale=0.25)
     out = run(w)
