@@ -1,7 +1,10 @@
 // partial.cu — the split-KV partial attention kernel (the hot loop).
 //
 // One persistent CTA per planner share of the flattened (sequence, kv head,
-// page) order. Its phases are the ones profiled on the page "[Kernel][SM70]
+// page) order, cut on the planner's cost line (each segment's switch cost
+// counted beside its pages; the CTA derives the plan itself from the context
+// lengths when the segment table fits in shared memory). Its phases are the
+// ones profiled on the page "[Kernel][SM70]
 // Pipeline batched E5M2 XQA decode" (section "Pending work and gates"): K load +
 // E5M2 conversion, shared-memory publication, QK, V load + conversion, PV and
 // synchronization. That page's starting kernel was memory-latency bound
@@ -35,12 +38,13 @@
 //     the fp16 P used for O).
 // A warp takes its pages two at a time, interleaving two independent
 // dependency chains (two-tile kernels load Q per segment instead of
-// prefetching it, to stay within 255 registers). At the end of a segment each warp hands its
-// (m, l, O) to a shared merge buffer and moves on; the buffered segments are
-// merged across warps when a buffer is reused and at the end of the range. A
-// segment owned whole by this CTA is normalised and written as fp16
-// (out = O * (v_scale / l)); a split piece goes to partial slot i + s, and the
-// CTA whose ticket completes the segment merges all its pieces.
+// prefetching it, to stay within 255 registers). At the end of a segment each
+// warp hands its (m, l, O) to a shared merge buffer and moves on; the buffered
+// segments are merged across warps when a buffer is reused and at the end of
+// the range. A segment owned whole by this CTA is normalised and written as
+// fp16 (out = O * (v_scale / l)); a split piece goes to partial slot i + s, and
+// the CTA whose ticket completes the segment merges all its pieces, loading
+// them (and those of its other completed segment) before using any.
 //
 // Contraction-index permutation: the MMA result does not depend on how the
 // contraction index is laid out, as long as both operands use the same layout.
