@@ -373,7 +373,7 @@ def run_gpu(args, world, rank, local, dist):
         per_step_us = sorted(edges[c].elapsed_time(edges[c + 1]) * 1e3 / ((bounds[c + 1] - bounds[c]) * C)
                              for c in range(n_chunks))
         repeats = {"n": n_chunks, "steps_each": (nrep // n_chunks) * C,
-                   "median_us": per_step_us[len(per_step_us) // 2],
+                   "median_us": _quantile(per_step_us, 0.5),
                    "p10_us": _quantile(per_step_us, 0.1), "p90_us": _quantile(per_step_us, 0.9)}
     ms_total_max = reduce_max(dist, ms_total)
     ms_per_step = ms_total_max / args.steps
