@@ -184,9 +184,8 @@ xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void
  *   seg_bad[B*Hkv]     = 1 where the segment's context length is invalid or a
  *                        bad block id was met, else 0 (may be NULL)
  *   seg_cost[B*Hkv]    = inclusive prefix sum of the segments' switch costs on
- *                        the cost line the CTAs are cut on: 0 for an empty
- *                        segment, 32 page units for one of fewer than 8 pages,
- *                        else 12 (may be NULL) */
+ *                        the cost line the CTAs are cut on: 32 page units per
+ *                        non-empty segment, 0 for an empty one (may be NULL) */
 xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int32_t* header,
                            int32_t* seg_start, int32_t* seg_bad, int32_t* seg_cost,
                            void* stream);

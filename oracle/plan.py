@@ -16,11 +16,10 @@ this build adopts (a reading) sizes every split from the total work:
 * the number of CTAs is ``n = 0`` if ``P == 0`` else
   ``min(max_ctas, max(1, ceil(P / min_pages_per_cta)))``;
 * the work is cut on a *cost line*: the segments are laid end to end, each
-  preceded by its switch cost ``seg_cost(pages)`` (0 for an empty segment,
-  32 for fewer than 8 pages, else 12, in page units: the measured time of a
-  segment switch inside a CTA of the GPU kernel, which the pages do not
-  state; with these costs a CTA holding many tiny segments no longer takes
-  several times longer than the rest); page ``p`` of segment ``s`` sits
+  preceded by its switch cost ``seg_cost(pages)`` (32 page units for a
+  non-empty segment, 0 for an empty one: a value tuned on the GPU kernel,
+  which the pages do not state; with it a CTA holding many tiny segments no
+  longer takes several times longer than the rest); page ``p`` of segment ``s`` sits
   at position ``p + cc[s]`` with ``cc[s]`` the sum of the costs of segments
   ``0..s``, and the line is ``V = P + cc[-1]`` long;
 * CTA ``i`` owns the positions ``[floor(i*V/n), floor((i+1)*V/n))`` and so
@@ -56,15 +55,13 @@ def segment_starts(pages) -> np.ndarray:
     return out
 
 
-SEG_COST_BIG = 12
-SEG_COST_SMALL = 32
-SMALL_SEG_PAGES = 8
+SEG_COST = 32
 
 
 def seg_cost(pages) -> np.ndarray:
     """Switch cost of each segment on the cost line, in page units."""
     pages = np.asarray(pages, dtype=np.int64)
-    return np.where(pages <= 0, 0, np.where(pages < SMALL_SEG_PAGES, SEG_COST_SMALL, SEG_COST_BIG))
+    return np.where(pages <= 0, 0, SEG_COST)
 
 
 def cost_prefix(seg_start) -> np.ndarray:

@@ -4,8 +4,8 @@
 // (sequence, kv head) segment as an exclusive prefix sum, the bad-segment
 // flags, the cost-line prefix, the total page count and the number of
 // partial-kernel CTAs. The cost line lays the segments end to end, each
-// preceded by its switch cost (seg_cost: 12 page units, 32 for a segment of
-// fewer than 8 pages); CTA i of the partial kernel owns the pages at positions
+// preceded by its switch cost (seg_cost: 32 page units for a non-empty
+// segment); CTA i of the partial kernel owns the pages at positions
 // [floor(i*V/n), floor((i+1)*V/n)) of that line. Every CTA gets the same cost
 // whatever the length mix: long sequences are split across CTAs, short ones
 // share a CTA, and many tiny segments are spread over several. This answers the two failure

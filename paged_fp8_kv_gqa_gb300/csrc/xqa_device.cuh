@@ -44,13 +44,11 @@ struct PartialGeom {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 constexpr int kDefaultMinPagesPerCta = 16;
-// Split rule cost line: every non-empty segment costs seg_cost(pages) page
-// units on top of its pages (the measured time of a segment switch inside a
-// CTA: about 12 pages' worth of streaming; a segment of fewer than 8 pages also
-// leaves most warps idle and costs about 32).
-constexpr int kSegCostBig = 12;
-constexpr int kSegCostSmall = 32;
-constexpr int kSmallSegPages = 8;
+// Split rule cost line: every non-empty segment costs kSegCost page units on
+// top of its pages (a segment switch inside a CTA, and the split-piece merge
+// work that falls on CTAs holding segment boundaries; the value minimises the
+// step time of the B8, B16 and mixed-length workloads, swept over 0..48).
+constexpr int kSegCost = 32;
 constexpr int kPlanThreads = 256;  // small enough to share an SM with a partial CTA
 constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
 
@@ -263,39 +261,18 @@ __host__ __device__ inline int num_ctas_for(int total_pages, int n_max, int min_
   return n < n_max ? n : n_max;
 }
 
-// CTA owning flattened page p when P pages are split over n CTAs.
-__host__ __device__ inline int cta_of_page(long long page, long long total, long long n) {
-  return (int)(((page + 1) * n - 1) / total);
-}
-
 // The cost line. Segment s (pages segs[s] .. segs[s+1]) costs
 // seg_cost(pages) units before its pages; cc[s] = sum of the costs of
 // segments 0..s. Page p of segment s sits at position p + cc[s], the line is
 // V = P + cc[nseg - 1] long, CTA i takes the positions [floor(iV/n),
 // floor((i+1)V/n)) and so a contiguous (possibly empty) run of pages.
-__host__ __device__ inline int seg_cost(int pages) {
-  return pages <= 0 ? 0 : (pages < kSmallSegPages ? kSegCostSmall : kSegCostBig);
-}
+__host__ __device__ inline int seg_cost(int pages) { return pages <= 0 ? 0 : kSegCost; }
 
 // CTA owning position v of a line of length V split over n CTAs.
 __host__ __device__ inline int cta_of_vpos(long long v, long long line, long long n) {
   return (int)(((v + 1) * n - 1) / line);
 }
 
-// The first page at a position >= a (P when there is none): the first
-// segment whose pages end past a on the line, then the offset into it.
-__host__ __device__ inline int page_of_vpos(const int32_t* segs, const int32_t* cc, int nseg,
-                                            long long a) {
-  int lo = 0, hi = nseg;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if ((long long)segs[mid + 1] + cc[mid] > a) hi = mid;
-    else lo = mid + 1;
-  }
-  if (lo == nseg) return segs[nseg];
-  const long long first = (long long)segs[lo] + cc[lo];
-  return a <= first ? segs[lo] : (int)(segs[lo] + (a - first));
-}
 
 // Device-scope fetch-and-add with acquire-release ordering.
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {

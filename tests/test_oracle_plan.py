@@ -39,7 +39,7 @@ def test_partition_brute_force(seed):
     mbs = int(rng.integers(1, 40))
     ctx = rng.integers(0, mbs * 16 + 1, size=B)
     ctx[rng.random(B) < 0.2] = 0
-    small = rng.random(B) < 0.3  # segments of fewer than 8 pages cost more
+    small = rng.random(B) < 0.3  # many short segments: the switch cost dominates
     ctx[small] = np.minimum(rng.integers(1, 8 * 16, size=int(small.sum())), mbs * 16)
     max_ctas = int(rng.integers(1, 160))
     minp = int(rng.integers(1, 12))
@@ -47,7 +47,7 @@ def test_partition_brute_force(seed):
     starts, total, n, cc = p["seg_start"], p["total_pages"], p["num_ctas"], p["seg_cc"]
     pages = np.diff(starts)
     assert np.array_equal(pages, np.repeat((ctx + 15) // 16, hkv))
-    costs = np.where(pages == 0, 0, np.where(pages < 8, 32, 12))
+    costs = np.where(pages == 0, 0, 32)
     assert np.array_equal(cc, np.cumsum(costs))
     if total == 0:
         assert n == 0
@@ -90,12 +90,12 @@ def test_tiny_segments_are_spread_over_ctas():
     assert len(set(owners)) >= 4
 
 
-def test_large_segments_cost_a_fixed_amount():
+def test_every_segment_costs_a_fixed_amount():
     # two equal long segments over two CTAs: the cut lands mid-line, i.e. in
     # the middle of the pages once both switch costs are counted
     p = plan.plan([16 * 100, 16 * 100], 1, 100, 2, 1)
     starts, cc, n = p["seg_start"], p["seg_cc"], p["num_ctas"]
-    assert list(cc) == [12, 24]
+    assert list(cc) == [32, 64]
     assert plan.cta_range(0, starts, cc, 2) == (0, 100)
     assert plan.cta_range(1, starts, cc, 2) == (100, 200)
 
