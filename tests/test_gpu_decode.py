@@ -9,6 +9,8 @@ inputs (the changed-input graph replays on the page "[Kernel][WIP] Follow up
 FlashNext batch HC fusion and QSA route audit", section "Test Result"),
 determinism, and the device-side error paths.
 """
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -110,6 +112,23 @@ def test_ctas_with_only_switch_cost_on_the_line(merge_mode):
     assert len(empty) > 0
     out = run(w, max_ctas=300, min_pages=1, merge_mode=merge_mode)
     assert_close(out, oracle_of(w), "empty cost-line shares")
+
+
+@functools.lru_cache(maxsize=None)
+def _long_sequence(q_len: int):
+    # one 131 072-token sequence: every kv head's segment is split over about
+    # 38 CTAs, so the final merge takes its pieces in several batches
+    w = wl.make_custom([131072], 32, 4, seed=63, q_len=q_len)
+    return w, oracle_of(w)
+
+
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_one_long_sequence_split_over_every_cta(q_len):
+    w, ref = _long_sequence(q_len)
+    a = run(w, merge_mode=0)
+    b = run(w, merge_mode=1)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    assert_close(a, ref, f"one 128K sequence, {q_len} new tokens")
 
 
 def test_single_token_context_is_the_v_row_bitwise():
