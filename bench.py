@@ -264,7 +264,13 @@ def run_gpu(args, world, rank, local, dist):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = workloads.make_workload(args.workload, kv_dtype=args.kv_dtype, q_len=args.q_len)
+    if args.contexts:  # a custom length mix with the same recipe (not the headline)
+        hq, hkv = (int(x) for x in args.heads.split(","))
+        w = workloads.make_custom([int(c) for c in args.contexts.split(",")], hq, hkv, seed=7,
+                                  kv_dtype=args.kv_dtype, q_len=args.q_len)
+        args.workload = f"custom contexts {args.contexts}, {hq}/{hkv} heads"
+    else:
+        w = workloads.make_workload(args.workload, kv_dtype=args.kv_dtype, q_len=args.q_len)
     if args.kv_layout == "nhd":
         w = workloads.to_nhd(w)
     kv_bytes = w.kv_bytes
@@ -442,7 +448,11 @@ def run_gpu(args, world, rank, local, dist):
         return None
     peak, peak_kind = hbm_peak()
     achieved = kv_bytes / (part_avg_ms * 1e-3) / 1e9
-    traffic = profiled_traffic()
+    # the committed capture is of the default configuration only
+    profiled_config = (not args.contexts and args.workload == DEFAULT_WORKLOAD
+                       and args.kv_dtype == "e5m2" and args.kv_layout == "hnd"
+                       and args.q_len == 1 and args.merge_mode == 0 and args.min_pages == 0)
+    traffic = profiled_traffic() if profiled_config else None
     value = aggregate_throughput(kv_bytes * args.steps, world, ms_total_max * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -494,7 +504,7 @@ def run_gpu(args, world, rank, local, dist):
         "e2e": e2e,
         "device_status": status,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not args.contexts:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     return line
 
@@ -594,6 +604,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=("xqa", "reference"), default="xqa")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--contexts", default="",
+                    help="comma-separated context lengths of a custom workload (with --heads)")
+    ap.add_argument("--heads", default="32,4", help="q heads,kv heads of a custom workload")
     ap.add_argument("--pools", type=int, default=4)
     ap.add_argument("--graph-steps", type=int, default=50)
     ap.add_argument("--event-every", type=int, default=10,
