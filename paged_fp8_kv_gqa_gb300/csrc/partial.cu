@@ -483,7 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int scan_warp[kWarps], scan_warp_cost[kWarps];
   __shared__ int scan_carry, scan_carry_cost;
   __shared__ long long cost_line;  // kept here: the end of the kernel reads it back
-  __shared__ int range_lo, range_hi, range_seg;  // this CTA's pages, first segment
+  __shared__ int range_lo, range_hi, range_seg, range_seg_hi;  // pages; first, last segment
+  __shared__ const int32_t* cc_base;  // the cost-line prefix the end of the kernel reads
   // split pieces of this CTA (at most its first and last segment), whose
   // merge tickets are taken once the whole range is done
   __shared__ int pend_seg[2], pend_poison[2], pend_last[2];
@@ -576,10 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // ---- rows of empty segments (context length 0, or invalid -> NaN) ----
-  if (cta == 0) {
+  // ---- rows of empty segments (context length 0, or invalid -> NaN), the
+  // segments spread over every warp of every CTA (a few each) ----
+  {
     const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
-    for (int s = warp; s < nseg; s += kWarps) {
+    for (int s = cta * kWarps + warp; s < nseg; s += gridDim.x * kWarps) {
       if (segs[s] != segs[s + 1]) continue;
       const int ctx = __ldg(&p.context_lens[s / p.num_kv_heads]);
       const bool bad = ctx < 0 || (long long)ctx > max_ctx;
@@ -603,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cost_line = line;
     range_lo = range_hi = total;  // no segment ends past the position
     range_seg = nseg;
+    range_seg_hi = nseg - 1;
     for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -618,21 +621,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       range_lo = vlo <= first ? segs[s] : (int)(segs[s] + (vlo - first));
       range_seg = s;
     }
-    if (end > vhi && prev <= vhi) range_hi = vhi <= first ? segs[s] : (int)(segs[s] + (vhi - first));
+    if (end > vhi && prev <= vhi) {
+      range_hi = vhi <= first ? segs[s] : (int)(segs[s] + (vhi - first));
+      range_seg_hi = s;  // the range's last segment is this one or an earlier one
+    }
   }
   __syncthreads();
   const int cbeg = range_lo, cend = range_hi;
   const int npages = cend - cbeg;
   if (npages <= 0) return;  // its share of the line is segment switch cost only
   const int s_first = range_seg;
+  // With the planner's table in global memory, the few segments this range
+  // touches (a contiguous run) are copied into the shared caches, and the
+  // table pointers are shifted so that segment s still reads entry s.
+  int s_hi = nseg - 1;  // the last segment any lookup of this range can reach
+  const int32_t* ctxs = segs_in_smem ? ctx_cache : p.context_lens;
+  if (!segs_in_smem) {
+    const int wn = range_seg_hi - s_first + 1;
+    const int b_first = s_first / p.num_kv_heads;
+    const int wb = range_seg_hi / p.num_kv_heads - b_first + 1;
+    if (wn + 1 <= kSegCache && wb <= kSegCache) {
+      for (int i = tid; i <= wn; i += kThreads) {
+        seg_cache[i] = segs[s_first + i];
+        if (i < wn) cc_cache[i] = cc[s_first + i];
+      }
+      for (int i = tid; i < wb; i += kThreads) ctx_cache[i] = __ldg(&p.context_lens[b_first + i]);
+      __syncthreads();
+      segs = seg_cache - s_first;
+      cc = cc_cache - s_first;
+      ctxs = ctx_cache - b_first;
+      s_hi = range_seg_hi;
+    }
+  }
+  if (tid == 0) cc_base = cc;
   volatile int* abort = &abort_flag;
   const uint64_t policy = l2_evict_first_policy();
   const int g = lane >> 2, c = lane & 3;
 
   // ---- this warp's loads: owned page k is CTA-local page warp + 8k ----
   const int owned = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
-  PageBatch cur = load_batch(p, segs, s_first, nseg, cbeg, npages, warp, 0, lane);
-  PageBatch nxt = load_batch(p, segs, s_first, nseg, cbeg, npages, warp, 32, lane);
+  PageBatch cur = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 0, lane);
+  PageBatch nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 32, lane);
   int cur_base = 0;
   int issued = 0;  // owned pages whose loads have been issued
   auto issue_next = [&]() {
@@ -641,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (k >= cur_base + 32) {
       cur = nxt;
       cur_base += 32;
-      nxt = load_batch(p, segs, s_first, nseg, cbeg, npages, warp, cur_base + 32, lane);
+      nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, cur_base + 32, lane);
     }
     const int y = __shfl_sync(kFull, cur.y, k - cur_base);
     const int bad = __shfl_sync(kFull, cur.bad, k - cur_base);
@@ -744,9 +773,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sb = segs[s], se = segs[s + 1];
     const int qe = min(se, cend) - cbeg;
     const int b = s / p.num_kv_heads;
-    // from shared memory when the plan was computed here: no global round trip
-    // at a segment switch
-    const int ctx = segs_in_smem ? ctx_cache[b] : __ldg(&p.context_lens[b]);
+    // from shared memory (the whole table, or this range's window of it): no
+    // global round trip at a segment switch
+    const int ctx = ctxs[b];
     const bool whole = (sb >= cbeg) && (se <= cend);
     if (kPrefetchQ && q_next_seg == s) {
 #pragma unroll
@@ -757,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_q<NT>(p, s, g, c, qf);
     }
     if (kPrefetchQ && qe < npages) {  // prefetch Q of the next segment this CTA works on
-      q_next_seg = find_segment(segs, s, nseg, cbeg + qe);
+      q_next_seg = find_segment(segs, s, s_hi + 1, cbeg + qe);
       load_q<NT>(p, q_next_seg, g, c, qf_next);
     }
     SegLimits<NT> sl;
@@ -875,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // order, exactly as the combine kernel would.
   if (npend > 0) {
     // the cost line again, read back rather than kept live through the loop
-    const int32_t* cc = segs_in_smem ? cc_cache : p.seg_cc;
+    const int32_t* cc = cc_base;
     const long long line = *reinterpret_cast<volatile long long*>(&cost_line);
     griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
     consumer_bar();  // all of this CTA's partial-slot writes precede the tickets

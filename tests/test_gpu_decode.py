@@ -39,14 +39,17 @@ def test_in_kernel_merge_equals_combine_kernel_bitwise(name):
 
 
 @pytest.mark.parametrize("merge_mode", [0, 1])
-def test_large_batch_plan_read_from_planner(merge_mode):
+@pytest.mark.parametrize("max_ctas", [0, 1])
+def test_large_batch_plan_read_from_planner(merge_mode, max_ctas):
     # 700 sequences x 4 kv heads: the segment table no longer fits in shared
-    # memory, so the partial kernel reads the planner's table instead
+    # memory, so the partial kernel reads the planner's table and copies its
+    # range's window of it into shared memory; with a single CTA the window is
+    # the whole table, too large, and the kernel reads the table in place
     rng = np.random.default_rng(77)
     ctx = rng.integers(0, 120, size=700)
     ctx[::37] = 0
     w = wl.make_custom(ctx, 32, 4, seed=77)
-    assert_close(run(w, merge_mode=merge_mode), oracle_of(w), "large batch")
+    assert_close(run(w, merge_mode=merge_mode, max_ctas=max_ctas), oracle_of(w), "large batch")
 
 
 @pytest.mark.parametrize("name", ["b4_uniform_ctx1024", "b12_boundary"])
