@@ -952,6 +952,716 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The same kernel with a second way to work a range (warp mode): when the
+// range touches at least kWarpModeMinPieces segment pieces of at most
+// kWarpModePages pages each, whole pieces go to single warps (round-robin over
+// the range's segments, a static rule), each warp accumulates its piece alone
+// and writes it from registers, with no merge across warps and no CTA barrier
+// per segment; other ranges are worked as above. Launched only for shapes with
+// many segments per CTA (batches of many short sequences): the extra code
+// slows the page loop of ranges worked the usual way.
+template <int kFmt, int NT, bool kMulti>
+__global__ void __launch_bounds__(kThreads, 1)
+    partial_kernel_wm(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const PartialParams p) {
+  using Geom = PartialGeom<NT>;
+  constexpr int kCols = Geom::kCols;
+  constexpr int kBufs = Geom::kMergeBufs;
+  constexpr bool kPairs = true;  // two pages per warp iteration
+  constexpr bool kPrefetchQ = NT == 1;  // registers: two-tile kernels load Q per segment
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ int stage_bad[kStages];
+  __shared__ int abort_flag;
+
+  __shared__ int scan_warp[kWarps], scan_warp_cost[kWarps];
+  __shared__ int scan_carry, scan_carry_cost;
+  __shared__ long long cost_line;  // kept here: the end of the kernel reads it back
+  __shared__ int range_lo, range_hi, range_seg, range_seg_hi;  // pages; first, last segment
+  __shared__ const int32_t* cc_base;  // the cost-line prefix the end of the kernel reads
+  // split pieces of this CTA (at most its first and last segment), whose
+  // merge tickets are taken once the whole range is done
+  __shared__ int pend_seg[2], pend_poison[2], pend_last[2];
+  __shared__ int npend;
+  // the segment each merge buffer holds, whether this CTA owns it whole, and
+  // each warp's "met a bad page" flag for it
+  __shared__ int buf_seg[kBufs], buf_whole[kBufs], buf_poison[kBufs][kWarps];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cta = blockIdx.x;
+  griddep_launch_dependents();  // a dependent next kernel waits for this grid itself
+  const int nseg = p.batch * p.num_kv_heads;
+  const int ncols = p.group * p.q_len;
+  // per-tensor scales: host values, or device scalars read when the kernel runs
+  const float k_scale = p.k_scale_ptr ? __ldg(p.k_scale_ptr) : p.k_scale;
+  const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
+  const float scale_log2 = static_cast<float>(p.qk_scale_base * static_cast<double>(k_scale));
+
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* merge_bufs = reinterpret_cast<float*>(stages + kStages * kStageBytes);
+  int32_t* seg_cache = reinterpret_cast<int32_t*>(merge_bufs + kBufs * Geom::kMergeBufFloats);
+  int32_t* ctx_cache = seg_cache + kSegCache;  // context length per sequence
+  int32_t* cc_cache = ctx_cache + kSegCache;   // cost-line prefix per segment
+
+  // ---- the plan: computed here when the segment table fits in shared memory
+  // (same integer rule as the planner kernel), else read from the planner ----
+  const bool segs_in_smem = nseg + 1 <= kSegCache;
+  const int32_t* segs;
+  const int32_t* cc;
+  int total, n;
+  if (segs_in_smem) {
+    if (tid == 0) scan_carry = scan_carry_cost = 0;
+    __syncthreads();
+    const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
+    for (int base = 0; base < p.batch; base += kThreads) {
+      const int b = base + tid;
+      int pages = 0;
+      if (b < p.batch) {
+        const int ctx = __ldg(&p.context_lens[b]);
+        ctx_cache[b] = ctx;
+        pages = (ctx < 0 || (long long)ctx > max_ctx) ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
+      }
+      const int cost = seg_cost(pages);  // every kv head's segment of sequence b
+      int incl = pages, incl_cost = cost;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(kFull, incl, off);
+        const int uc = __shfl_up_sync(kFull, incl_cost, off);
+        if (lane >= off) {
+          incl += u;
+          incl_cost += uc;
+        }
+      }
+      if (lane == 31) {
+        scan_warp[warp] = incl;
+        scan_warp_cost[warp] = incl_cost;
+      }
+      __syncthreads();
+      int before = scan_carry, before_cost = scan_carry_cost;
+      for (int w = 0; w < warp; ++w) {
+        before += scan_warp[w];
+        before_cost += scan_warp_cost[w];
+      }
+      const int excl = before + incl - pages;
+      const int excl_cost = before_cost + incl_cost - cost;
+      if (b < p.batch)
+        for (int h = 0; h < p.num_kv_heads; ++h) {
+          seg_cache[b * p.num_kv_heads + h] = excl * p.num_kv_heads + h * pages;
+          cc_cache[b * p.num_kv_heads + h] = excl_cost * p.num_kv_heads + (h + 1) * cost;
+        }
+      __syncthreads();
+      if (tid == kThreads - 1) {
+        scan_carry = excl + pages;
+        scan_carry_cost = excl_cost + cost;
+      }
+      __syncthreads();
+    }
+    total = scan_carry * p.num_kv_heads;
+    if (tid == 0) seg_cache[nseg] = total;
+    n = num_ctas_for(total, p.n_max, p.min_pages);
+    segs = seg_cache;
+    cc = cc_cache;
+  } else {
+    griddep_wait();
+    total = p.header[2];
+    n = p.header[1];
+    segs = p.seg_start;
+    cc = p.seg_cc;
+  }
+  __syncthreads();
+
+  // ---- rows of empty segments (context length 0, or invalid -> NaN), the
+  // segments spread over every warp of every CTA (a few each) ----
+  {
+    const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
+    for (int s = cta * kWarps + warp; s < nseg; s += gridDim.x * kWarps) {
+      if (segs[s] != segs[s + 1]) continue;
+      const int ctx = __ldg(&p.context_lens[s / p.num_kv_heads]);
+      const bool bad = ctx < 0 || (long long)ctx > max_ctx;
+      const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
+      uint4 val;
+      val.x = val.y = val.z = val.w = pack_half2(v, v);
+      for (int i = lane; i < ncols * (kHeadDim / 8); i += 32) {
+        const int col = i / (kHeadDim / 8), d8 = i - col * (kHeadDim / 8);
+        reinterpret_cast<uint4*>(p.out + col_row(p, s, col) * kHeadDim)[d8] = val;
+      }
+    }
+  }
+  if (cta >= n) return;
+  // This CTA's positions [vlo, vhi) on the cost line, and the pages there: the
+  // first page at a position >= a lies in the first segment whose pages end
+  // past a. One parallel pass over the segments finds both ends (and the
+  // first segment) in shared memory, in place of two dependent searches.
+  const long long line = (long long)total + (nseg > 0 ? cc[nseg - 1] : 0);
+  const long long vlo = ((long long)cta * line) / n, vhi = ((long long)(cta + 1) * line) / n;
+  if (tid == 0) {
+    cost_line = line;
+    range_lo = range_hi = total;  // no segment ends past the position
+    range_seg = nseg;
+    range_seg_hi = nseg - 1;
+    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
+    abort_flag = 0;
+    npend = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  __syncthreads();
+  for (int s = tid; s < nseg; s += kThreads) {
+    const long long end = (long long)segs[s + 1] + cc[s];                 // past its last page
+    const long long prev = s > 0 ? (long long)segs[s] + cc[s - 1] : -1;  // previous one's end
+    const long long first = (long long)segs[s] + cc[s];                   // its first page
+    if (end > vlo && prev <= vlo) {
+      range_lo = vlo <= first ? segs[s] : (int)(segs[s] + (vlo - first));
+      range_seg = s;
+    }
+    if (end > vhi && prev <= vhi) {
+      range_hi = vhi <= first ? segs[s] : (int)(segs[s] + (vhi - first));
+      range_seg_hi = s;  // the range's last segment is this one or an earlier one
+    }
+  }
+  __syncthreads();
+  const int cbeg = range_lo, cend = range_hi;
+  const int npages = cend - cbeg;
+  if (npages <= 0) return;  // its share of the line is segment switch cost only
+  const int s_first = range_seg;
+  // With the planner's table in global memory, the few segments this range
+  // touches (a contiguous run) are copied into the shared caches, and the
+  // table pointers are shifted so that segment s still reads entry s.
+  int s_hi = nseg - 1;  // the last segment any lookup of this range can reach
+  const int32_t* ctxs = segs_in_smem ? ctx_cache : p.context_lens;
+  if (!segs_in_smem) {
+    const int wn = range_seg_hi - s_first + 1;
+    const int b_first = s_first / p.num_kv_heads;
+    const int wb = range_seg_hi / p.num_kv_heads - b_first + 1;
+    if (wn + 1 <= kSegCache && wb <= kSegCache) {
+      for (int i = tid; i <= wn; i += kThreads) {
+        seg_cache[i] = segs[s_first + i];
+        if (i < wn) cc_cache[i] = cc[s_first + i];
+      }
+      for (int i = tid; i < wb; i += kThreads) ctx_cache[i] = __ldg(&p.context_lens[b_first + i]);
+      __syncthreads();
+      segs = seg_cache - s_first;
+      cc = cc_cache - s_first;
+      ctxs = ctx_cache - b_first;
+      s_hi = range_seg_hi;
+    }
+  }
+  if (tid == 0) cc_base = cc;
+  volatile int* abort = &abort_flag;
+  const uint64_t policy = l2_evict_first_policy();
+  const int g = lane >> 2, c = lane & 3;
+
+
+  WarpState<NT> st;
+  uint32_t qf[NT][16], qf_next[NT][16];
+  int q_next_seg = -1;
+  // Merge of one buffered segment by all threads (column col, dims dq..dq+3):
+  // the 8 warps' (m, l, O) combine in shared memory; a segment owned whole is
+  // normalised and written as fp16, a split piece goes to partial slot cta + s.
+  auto merge_buffer = [&](int mb) {
+    const int ms = buf_seg[mb];
+    const bool mwhole = buf_whole[mb] != 0;
+    int any_poison = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) any_poison |= buf_poison[mb][w];
+    const float* base = merge_bufs + mb * Geom::kMergeBufFloats;
+    const float* bm = base + Geom::kScratchFloats;
+    const float* bl = bm + kWarps * kCols;
+    const int dq = (tid & 31) * 4;  // 0..124
+#pragma unroll
+    for (int col = tid >> 5; col < kCols; col += kWarps) {
+      if (col >= ncols) break;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, bm[w * kCols + col]);
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = bm[w * kCols + col];
+        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        L += sc * bl[w * kCols + col];
+        const float4 v =
+            *reinterpret_cast<const float4*>(base + (w * kCols + col) * kScratchStride + dq);
+        acc.x += sc * v.x;
+        acc.y += sc * v.y;
+        acc.z += sc * v.z;
+        acc.w += sc * v.w;
+      }
+      if (mwhole) {
+        __half* o = p.out + col_row(p, ms, col) * kHeadDim + dq;
+        if (any_poison) {
+          const float nan = __int_as_float(0x7fc00000);
+          store_half4(o, nan, nan, nan, nan);
+        } else {
+          const float rr = (L > 0.f) ? v_scale / L : 0.f;
+          store_half4(o, acc.x * rr, acc.y * rr, acc.z * rr, acc.w * rr);
+        }
+      } else {
+        float* slotp = p.partials + (size_t)(cta + ms) * kSlotFloats;
+        *reinterpret_cast<float4*>(slotp + col * kHeadDim + dq) = acc;
+        if (dq == 0) {
+          slotp[kSlotM + col] = M;
+          slotp[kSlotL + col] = L;
+        }
+      }
+    }
+    if (!mwhole && tid == 0) {  // a split piece: its ticket is taken after the range
+      pend_seg[npend] = ms;
+      pend_poison[npend] = any_poison;
+      ++npend;
+    }
+  };
+
+  int issued = 0;  // this warp's pages whose loads have been issued
+  int kseg = 0;    // pieces handed to the merge buffers
+
+  // ---- mode: a range of at least kWarpModeMinPieces segment pieces of at
+  // most kWarpModePages pages each is worked in warp mode: whole pieces go to
+  // single warps (round-robin over the range's segments, a static rule), each
+  // accumulates its piece alone and writes it from registers, with no merge
+  // across warps and no CTA barrier per segment. Otherwise every warp takes
+  // every eighth page of the range (CTA mode). ----
+  const int nsr = find_segment(segs, s_first, s_hi + 1, cend - 1) - s_first + 1;  // segments touched
+  bool warp_mode = false;
+  if (NT == 1 && nsr >= kWarpModeMinPieces && nsr <= kThreads) {
+    int len = 0;
+    if (tid < nsr) len = min(segs[s_first + tid + 1], cend) - max(segs[s_first + tid], cbeg);
+    const int pieces = __syncthreads_count(len > 0);
+    const int too_long = __syncthreads_or(len > kWarpModePages);
+    warp_mode = pieces >= kWarpModeMinPieces && !too_long;
+  }
+
+  if (!warp_mode) {
+    // ---- this warp's loads: owned page k is CTA-local page warp + 8k ----
+    const int owned = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
+    PageBatch cur = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 0, lane);
+    PageBatch nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 32, lane);
+    int cur_base = 0;
+    auto issue_next = [&]() {
+      if (issued >= owned) return;
+      const int k = issued++;
+      if (k >= cur_base + 32) {
+        cur = nxt;
+        cur_base += 32;
+        nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, cur_base + 32, lane);
+      }
+      const int y = __shfl_sync(kFull, cur.y, k - cur_base);
+      const int bad = __shfl_sync(kFull, cur.bad, k - cur_base);
+      const int sg = __shfl_sync(kFull, cur.seg, k - cur_base);
+      const int slot = (warp + kWarps * k) % kStages;
+      __syncwarp();  // all lanes' reads of this slot's previous page are done
+      if (lane == 0) {
+        uint8_t* st = stages + slot * kStageBytes;
+        stage_bad[slot] = bad;
+        fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
+        if (bad) {
+          griddep_wait();  // the planner resets seg_bad and the status word
+          atomicOr(&p.seg_bad[sg], 1);
+          record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
+          mbar_arrive(&full_bar[slot]);
+        } else {
+          mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
+          if (p.kv_layout == XQA_LAYOUT_HND) {
+            tma_load_2d(st, &tm_k, &full_bar[slot], 0, y, policy);
+            tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, y, policy);
+          } else {  // NHD: box (128 dims, 1 kv head, 16 tokens) at (0, kvh, page*16)
+            const int kvh = sg - (sg / p.num_kv_heads) * p.num_kv_heads;
+            tma_load_3d(st, &tm_k, &full_bar[slot], 0, kvh, y, policy);
+            tma_load_3d(st + kPageBytes, &tm_v, &full_bar[slot], 0, kvh, y, policy);
+          }
+        }
+      }
+      __syncwarp();
+    };
+#pragma unroll 1
+    for (int i = 0; i < kLookahead; ++i) issue_next();
+
+    int s = s_first;
+    int q0 = 0;
+    while (q0 < npages) {
+      while (segs[s + 1] <= cbeg + q0) ++s;
+      const int sb = segs[s], se = segs[s + 1];
+      const int qe = min(se, cend) - cbeg;
+      const int b = s / p.num_kv_heads;
+      // from shared memory (the whole table, or this range's window of it): no
+      // global round trip at a segment switch
+      const int ctx = ctxs[b];
+      const bool whole = (sb >= cbeg) && (se <= cend);
+      if (kPrefetchQ && q_next_seg == s) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) qf[j][i] = qf_next[j][i];
+      } else {
+        load_q<NT>(p, s, g, c, qf);
+      }
+      if (kPrefetchQ && qe < npages) {  // prefetch Q of the next segment this CTA works on
+        q_next_seg = find_segment(segs, s, s_hi + 1, cbeg + qe);
+        load_q<NT>(p, q_next_seg, g, c, qf_next);
+      }
+      SegLimits<NT> sl;
+      sl.min_lim = ctx - p.q_len;  // the first new token's last visible token
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = 8 * j + 2 * c + e;
+          sl.lim[j][e] = col < ncols ? ctx - p.q_len + col / p.group : 0x7fffffff;
+        }
+      reset_state<NT>(st);
+      int poisoned = 0;
+
+      // this warp's pages of the segment (q, and q + kWarps when pairing)
+      for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe;
+           q += (kPairs ? 2 : 1) * kWarps) {
+        const bool pair = kPairs && q + kWarps < qe;
+        const int slot0 = q % kStages, slot1 = (q + kWarps) % kStages;
+        bool ready = mbar_wait_bounded(&full_bar[slot0], (q / kStages) & 1, abort);
+        if (pair) ready = ready && mbar_wait_bounded(&full_bar[slot1], ((q + kWarps) / kStages) & 1, abort);
+        if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
+          poisoned = 1;
+          if (lane == 0) {
+            *abort = 1;
+            griddep_wait();
+            record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
+          }
+          continue;
+        }
+        const uint8_t* stg0 = stages + slot0 * kStageBytes;
+        const uint8_t* stg1 = stages + slot1 * kStageBytes;
+        const bool bad0 = stage_bad[slot0] != 0, bad1 = pair && stage_bad[slot1] != 0;
+        PageRegs regs[2];
+        regs[0] = load_page(stg0, stg0 + kPageBytes, g, c);
+        if (pair) regs[1] = load_page(stg1, stg1 + kPageBytes, g, c);
+        // The pages are in registers: refill their slots with the pages kStages
+        // ahead right away (warp-uniform decision), before the math.
+        if (!__any_sync(kFull, *abort != 0)) {
+          issue_next();
+          if (pair) issue_next();
+        }
+        const int j0 = cbeg + q - sb;  // page index within the sequence
+        const int t0 = j0 * kBlockSize, t1 = (j0 + kWarps) * kBlockSize;
+        const int nv0 = min(kBlockSize, ctx - t0), nv1 = min(kBlockSize, ctx - t1);
+        if (kPairs && pair && !bad0 && !bad1) {
+          const int tk[2] = {t0, t1}, nv[2] = {nv0, nv1};
+          process_pages<kFmt, 2, NT, kMulti>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
+        } else {
+          if (bad0 || bad1) poisoned = 1;
+          if (!bad0) {
+            const PageRegs one[1] = {regs[0]};
+            const int tk[1] = {t0}, nv[1] = {nv0};
+            process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
+          }
+          if (pair && !bad1) {
+            const PageRegs one[1] = {regs[1]};
+            const int tk[1] = {t1}, nv[1] = {nv1};
+            process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
+          }
+        }
+      }
+
+      // ---- hand this segment's per-warp state to a merge buffer; a CTA-wide
+      // barrier only when the buffer still holds an unmerged segment (with two
+      // buffers a range of at most two segments never stops mid-way) ----
+      const int buf = kseg % kBufs;
+      if (kseg >= kBufs) {
+        consumer_bar();
+        merge_buffer(buf);
+        consumer_bar();
+      }
+      {
+        float* base = merge_bufs + buf * Geom::kMergeBufFloats;
+        float* bm = base + Geom::kScratchFloats;
+        float* bl = bm + kWarps * kCols;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          float* my = base + (warp * kCols + 8 * j) * kScratchStride;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int d0 = 16 * g + 2 * i;
+            my[(2 * c) * kScratchStride + d0] = st.o[j][i][0];
+            my[(2 * c + 1) * kScratchStride + d0] = st.o[j][i][1];
+            my[(2 * c) * kScratchStride + d0 + 1] = st.o[j][i][2];
+            my[(2 * c + 1) * kScratchStride + d0 + 1] = st.o[j][i][3];
+          }
+          if (g == 0) {
+            bm[warp * kCols + 8 * j + 2 * c] = st.m[j][0];
+            bm[warp * kCols + 8 * j + 2 * c + 1] = st.m[j][1];
+            bl[warp * kCols + 8 * j + 2 * c] = st.l[j][0];
+            bl[warp * kCols + 8 * j + 2 * c + 1] = st.l[j][1];
+          }
+        }
+        if (lane == 0) buf_poison[buf][warp] = poisoned;
+        if (tid == 0) {
+          buf_seg[buf] = s;
+          buf_whole[buf] = whole ? 1 : 0;
+        }
+      }
+      ++kseg;
+      q0 = qe;
+      ++s;
+    }
+  } else if constexpr (NT == 1) {
+    // ---- warp mode: this warp's pieces are the range's segments j = warp,
+    // warp + 8, ... (j counted from s_first; empty ones skipped). A piece's
+    // block ids are fetched one per lane; the next piece's when the current
+    // one starts issuing.
+    auto piece = [&](int j, int& pb, int& len) {
+      const int sg = s_first + j;
+      pb = max(segs[sg], cbeg);
+      len = min(segs[sg + 1], cend) - pb;
+    };
+    auto next_piece = [&](int j) {  // the first non-empty piece among j, j + 8, ...
+      for (; j < nsr; j += kWarps) {
+        int pb, len;
+        piece(j, pb, len);
+        if (len > 0) break;
+      }
+      return j;
+    };
+    auto fetch = [&](int j) {
+      PageBatch r{0, 0, 0};
+      if (j < nsr) {
+        int pb, len;
+        piece(j, pb, len);
+        const int sg = s_first + j;
+        r.seg = sg;
+        if (lane < len) {
+          const int bb = sg / p.num_kv_heads, kvh = sg - bb * p.num_kv_heads;
+          const int id =
+              __ldg(&p.block_tables[(size_t)bb * p.max_blocks_per_seq + (pb + lane - segs[sg])]);
+          r.bad = (id < 0 || id >= p.num_blocks) ? 1 : 0;
+          r.y = r.bad ? 0
+                      : (p.kv_layout == XQA_LAYOUT_HND ? (id * p.num_kv_heads + kvh) : id) * kBlockSize;
+        }
+      }
+      return r;
+    };
+    int ij = next_piece(warp), ioff = 0;  // the piece being issued, its next page
+    int ij_next = next_piece(ij + kWarps);
+    PageBatch wcur = fetch(ij), wnxt = fetch(ij_next);
+    auto issue_next_w = [&]() {
+      while (ij < nsr) {
+        int pb, len;
+        piece(ij, pb, len);
+        if (ioff < len) {
+          const int y = __shfl_sync(kFull, wcur.y, ioff);
+          const int bad = __shfl_sync(kFull, wcur.bad, ioff);
+          ++ioff;
+          const int k = issued++;
+          const int sg = wcur.seg;
+          const int slot = (warp + kWarps * k) % kStages;
+          __syncwarp();  // all lanes' reads of this slot's previous page are done
+          if (lane == 0) {
+            uint8_t* st = stages + slot * kStageBytes;
+            stage_bad[slot] = bad;
+            fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
+            if (bad) {
+              griddep_wait();  // the planner resets seg_bad and the status word
+              atomicOr(&p.seg_bad[sg], 1);
+              record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
+              mbar_arrive(&full_bar[slot]);
+            } else {
+              mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
+              if (p.kv_layout == XQA_LAYOUT_HND) {
+                tma_load_2d(st, &tm_k, &full_bar[slot], 0, y, policy);
+                tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, y, policy);
+              } else {  // NHD: box (128 dims, 1 kv head, 16 tokens) at (0, kvh, page*16)
+                const int kvh = sg - (sg / p.num_kv_heads) * p.num_kv_heads;
+                tma_load_3d(st, &tm_k, &full_bar[slot], 0, kvh, y, policy);
+                tma_load_3d(st + kPageBytes, &tm_v, &full_bar[slot], 0, kvh, y, policy);
+              }
+            }
+          }
+          __syncwarp();
+          return;
+        }
+        ij = ij_next;
+        ioff = 0;
+        wcur = wnxt;
+        ij_next = next_piece(ij + kWarps);
+        wnxt = fetch(ij_next);
+      }
+    };
+#pragma unroll 1
+    for (int i = 0; i < kLookahead; ++i) issue_next_w();
+
+    int k = 0;  // this warp's running page index (ring slot and phase)
+    for (int j = next_piece(warp); j < nsr; j = next_piece(j + kWarps)) {
+      const int s = s_first + j;
+      int pb, len;
+      piece(j, pb, len);
+      const int sb = segs[s], se = segs[s + 1];
+      const bool whole = (sb >= cbeg) && (se <= cend);
+      const int ctx = ctxs[s / p.num_kv_heads];
+      if (kPrefetchQ && q_next_seg == s) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qf[0][i] = qf_next[0][i];
+      } else {
+        load_q<NT>(p, s, g, c, qf);
+      }
+      if (kPrefetchQ) {  // Q of this warp's next piece
+        const int jn = next_piece(j + kWarps);
+        if (jn < nsr) {
+          q_next_seg = s_first + jn;
+          load_q<NT>(p, q_next_seg, g, c, qf_next);
+        }
+      }
+      SegLimits<NT> sl;
+      sl.min_lim = ctx - p.q_len;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = 2 * c + e;
+        sl.lim[0][e] = col < ncols ? ctx - p.q_len + col / p.group : 0x7fffffff;
+      }
+      reset_state<NT>(st);
+      int poisoned = 0;
+      for (int o = 0; o < len; o += 2) {
+        const bool pair = o + 1 < len;
+        const int slot0 = (warp + kWarps * k) % kStages, slot1 = (warp + kWarps * (k + 1)) % kStages;
+        bool ready = mbar_wait_bounded(&full_bar[slot0], (k / kLookahead) & 1, abort);
+        if (pair) ready = ready && mbar_wait_bounded(&full_bar[slot1], ((k + 1) / kLookahead) & 1, abort);
+        k += pair ? 2 : 1;
+        if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
+          poisoned = 1;
+          if (lane == 0) {
+            *abort = 1;
+            griddep_wait();
+            record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
+          }
+          continue;
+        }
+        const uint8_t* stg0 = stages + slot0 * kStageBytes;
+        const uint8_t* stg1 = stages + slot1 * kStageBytes;
+        const bool bad0 = stage_bad[slot0] != 0, bad1 = pair && stage_bad[slot1] != 0;
+        PageRegs regs[2];
+        regs[0] = load_page(stg0, stg0 + kPageBytes, g, c);
+        if (pair) regs[1] = load_page(stg1, stg1 + kPageBytes, g, c);
+        if (!__any_sync(kFull, *abort != 0)) {
+          issue_next_w();
+          if (pair) issue_next_w();
+        }
+        const int t0 = (pb + o - sb) * kBlockSize, t1 = t0 + kBlockSize;
+        const int nv0 = min(kBlockSize, ctx - t0), nv1 = min(kBlockSize, ctx - t1);
+        if (pair && !bad0 && !bad1) {
+          const int tk[2] = {t0, t1}, nv[2] = {nv0, nv1};
+          process_pages<kFmt, 2, NT, kMulti>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
+        } else {
+          if (bad0 || bad1) poisoned = 1;
+          if (!bad0) {
+            const PageRegs one[1] = {regs[0]};
+            const int tk[1] = {t0}, nv[1] = {nv0};
+            process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
+          }
+          if (pair && !bad1) {
+            const PageRegs one[1] = {regs[1]};
+            const int tk[1] = {t1}, nv[1] = {nv1};
+            process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
+          }
+        }
+      }
+      // ---- the piece's (m, l, O) straight from this warp's registers: lane
+      // (g, c) holds dims 16g + 2i (+1) of columns 2c, 2c + 1 ----
+      const float nan = __int_as_float(0x7fc00000);
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int col = 2 * c + e2;
+        if (col >= ncols) continue;
+        if (whole) {
+          __half* orow = p.out + col_row(p, s, col) * kHeadDim;
+          const float l = st.l[0][e2];
+          const float rr = poisoned ? nan : ((l > 0.f) ? v_scale / l : 0.f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int d0 = 16 * g + 2 * i;
+            *reinterpret_cast<uint32_t*>(orow + d0) =
+                pack_half2(st.o[0][i][e2] * rr, st.o[0][i][e2 + 2] * rr);
+          }
+        } else {
+          float* slotp = p.partials + (size_t)(cta + s) * kSlotFloats;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int d0 = 16 * g + 2 * i;
+            *reinterpret_cast<float2*>(slotp + col * kHeadDim + d0) =
+                make_float2(st.o[0][i][e2], st.o[0][i][e2 + 2]);
+          }
+          if (g == 0) {
+            slotp[kSlotM + col] = st.m[0][e2];
+            slotp[kSlotL + col] = st.l[0][e2];
+          }
+        }
+      }
+      if (!whole && lane == 0) {  // a split piece: its ticket is taken after all the work
+        const int idx = atomicAdd(&npend, 1);
+        pend_seg[idx] = s;
+        pend_poison[idx] = poisoned;
+      }
+    }
+  }
+
+  // ---- merges still buffered (the range's last kBufs segments), in order ----
+  consumer_bar();
+  for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k) merge_buffer(k % kBufs);
+  consumer_bar();
+
+  // ---- split pieces: flag, ticket, and merge by the CTA that finishes last ----
+  // The ticket (a device-wide atomic round trip) is taken once per piece after
+  // the whole range, so no mid-range segment boundary stalls the CTA on it.
+  // The CTA whose ticket completes a segment merges all its pieces in slot
+  // order, exactly as the combine kernel would.
+  if (npend > 0) {
+    // the cost line again, read back rather than kept live through the loop
+    const int32_t* cc = cc_base;
+    const long long line = *reinterpret_cast<volatile long long*>(&cost_line);
+    griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
+    consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
+    if (tid < npend) {
+      const int ps = pend_seg[tid];
+      if (pend_poison[tid]) atomicOr(&p.seg_bad[ps], 1);
+      int last = 0;
+      if (p.fused_merge) {
+        const int ilo = cta_of_vpos((long long)segs[ps] + cc[ps], line, n);
+        const int ihi = cta_of_vpos((long long)segs[ps + 1] - 1 + cc[ps], line, n);
+        // release: this CTA's slots (ordered before by the barrier) are visible
+        // to whoever takes a later ticket; acquire: the earlier pieces are
+        // visible to this CTA after the next barrier
+        last = (atom_add_acq_rel_gpu(&p.seg_count[ps], 1) == ihi - ilo) ? 1 : 0;
+      }
+      pend_last[tid] = last;
+    }
+    consumer_bar();
+    int m0 = 0, m1 = 0, nm = 0;  // the segments this CTA completes (at most two)
+    for (int i = 0; i < npend; ++i) {
+      if (!pend_last[i]) continue;
+      if (nm == 0) m0 = pend_seg[i];
+      else m1 = pend_seg[i];
+      ++nm;
+    }
+    const int ms[2] = {m0, m1};
+    if (nm > 0)
+      for (int col = tid >> 5; col < kCols; col += kWarps)
+        merge_segments<NT == 1>(p, ms, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
+  }
+
+  // Drain: after an abort some issued copies may not have been waited for; every
+  // copy must land before the CTA's shared memory is released.
+  if (*abort) {
+    int never = 0;
+    volatile int* no_abort = &never;
+    // only the last kLookahead issued pages can still be in flight: every
+    // earlier one was waited for before its slot was reissued
+    const int first = issued > kLookahead ? issued - kLookahead : 0;
+    for (int k = first; k < issued; ++k) {
+      const int q = warp + kWarps * k;
+      const bool ok = mbar_wait_bounded(&full_bar[q % kStages], (q / kStages) & 1, no_abort);
+      if (!__all_sync(kFull, ok)) break;
+    }
+  }
+}
+
 cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const PartialParams& p, int n_max, cudaStream_t stream) {
   // Programmatic dependent launch: CTAs may start while the planner (the
@@ -969,8 +1679,17 @@ cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // instances: (format) x (one tile, single token | one tile, several tokens |
-  // two tiles)
+  // two tiles); one-tile shapes with at least kWarpModeMinPieces segments per
+  // CTA take the warp-capable kernel
   const bool multi = p.q_len > 1;
+  const bool wm = nt == 1 && (long long)p.batch * p.num_kv_heads >= (long long)kWarpModeMinPieces * n_max;
+  if (wm) {
+    if (p.kv_dtype == XQA_KV_E4M3)
+      return multi ? cudaLaunchKernelEx(&cfg, partial_kernel_wm<XQA_KV_E4M3, 1, true>, tm_k, tm_v, p)
+                   : cudaLaunchKernelEx(&cfg, partial_kernel_wm<XQA_KV_E4M3, 1, false>, tm_k, tm_v, p);
+    return multi ? cudaLaunchKernelEx(&cfg, partial_kernel_wm<XQA_KV_E5M2, 1, true>, tm_k, tm_v, p)
+                 : cudaLaunchKernelEx(&cfg, partial_kernel_wm<XQA_KV_E5M2, 1, false>, tm_k, tm_v, p);
+  }
   if (p.kv_dtype == XQA_KV_E4M3) {
     if (nt == 2) return cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 2, true>, tm_k, tm_v, p);
     return multi ? cudaLaunchKernelEx(&cfg, partial_kernel<XQA_KV_E4M3, 1, true>, tm_k, tm_v, p)
@@ -990,7 +1709,11 @@ cudaError_t set_partial_attributes() {
   if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E5M2, 2, true>, a, s2)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 1, false>, a, s1)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 1, true>, a, s1)) != cudaSuccess) return e;
-  return cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 2, true>, a, s2);
+  if ((e = cudaFuncSetAttribute(partial_kernel<XQA_KV_E4M3, 2, true>, a, s2)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel_wm<XQA_KV_E5M2, 1, false>, a, s1)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel_wm<XQA_KV_E5M2, 1, true>, a, s1)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(partial_kernel_wm<XQA_KV_E4M3, 1, false>, a, s1)) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(partial_kernel_wm<XQA_KV_E4M3, 1, true>, a, s1);
 }
 
 }  // namespace xqa

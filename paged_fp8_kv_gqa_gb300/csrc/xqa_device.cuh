@@ -49,6 +49,10 @@ constexpr int kDefaultMinPagesPerCta = 16;
 // work that falls on CTAs holding segment boundaries; the value minimises the
 // step time of the B8, B16 and mixed-length workloads, swept over 0..48).
 constexpr int kSegCost = 32;
+// Warp mode of the partial kernel: a CTA range of at least this many segment
+// pieces, none longer than kWarpModePages pages, gives whole pieces to warps.
+constexpr int kWarpModeMinPieces = 4;
+constexpr int kWarpModePages = 32;
 constexpr int kPlanThreads = 256;  // small enough to share an SM with a partial CTA
 constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
 

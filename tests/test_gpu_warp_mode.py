@@ -1,0 +1,64 @@
+"""GPU parity of the partial kernel's warp mode (through the C ABI).
+
+Batches of many short sequences (at least four segments per CTA, none longer
+than 32 pages) are worked with whole segment pieces per warp instead of every
+eighth page per warp. Same tolerance as the other parity tests; the fused and
+the separate merge stay bitwise equal.
+"""
+import numpy as np
+import pytest
+
+import paged_fp8_kv_gqa_gb300 as xqa
+from gpu_helpers import Dev, assert_close, oracle_of, run, to_dev
+from paged_fp8_kv_gqa_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _short_batch(seed, hq=32, hkv=4, q_len=1, kv_dtype="e5m2", batch=160):
+    # 160 x 4 = 640 segments >= 4 per CTA on a 152-SM GPU; up to 25 pages each,
+    # some a single token, some exactly a page or two
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(1, 400, size=batch)
+    ctx[::17] = 16
+    ctx[5::23] = 1
+    ctx[7::29] = 32
+    ctx = np.maximum(ctx, q_len)
+    return wl.make_custom(ctx, hq, hkv, seed=seed, q_len=q_len, kv_dtype=kv_dtype)
+
+
+@pytest.mark.parametrize("kv_dtype", ["e5m2", "e4m3"])
+@pytest.mark.parametrize("hq,hkv,q_len", [(32, 4, 1), (16, 4, 2), (8, 8, 1)])
+def test_warp_mode_matches_oracle(kv_dtype, hq, hkv, q_len):
+    w = _short_batch(101 + hq + q_len, hq, hkv, q_len, kv_dtype, batch=160 if hkv == 4 else 80)
+    a = run(w, merge_mode=0)
+    b = run(w, merge_mode=1)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    assert_close(a, oracle_of(w), f"warp mode {kv_dtype} G={hq // hkv} T={q_len}")
+
+
+def test_warp_mode_nhd_equals_hnd_bitwise():
+    w = _short_batch(111)
+    assert np.array_equal(run(w).view(np.uint16), run(wl.to_nhd(w)).view(np.uint16))
+
+
+def test_warp_mode_relocation_and_determinism():
+    w = _short_batch(112)
+    a = run(w)
+    assert np.array_equal(a.view(np.uint16), run(w).view(np.uint16))
+    assert np.array_equal(a.view(np.uint16), run(wl.relocate_pages(w, seed=5)).view(np.uint16))
+
+
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_warp_mode_bad_block_id_is_contained(merge_mode):
+    w = _short_batch(113)
+    ref = oracle_of(w)
+    bad = 37
+    w.block_tables[bad, 0] = w.num_blocks + 3
+    d = Dev(w, merge_mode=merge_mode)
+    d.run()
+    out = d.result()
+    assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
+    assert np.all(np.isnan(out[bad].astype(np.float32)))
+    good = [b for b in range(w.batch) if b != bad]
+    assert_close(out[good], ref[good], "rows beside a bad block id (warp mode)")
