@@ -7,12 +7,43 @@ the separate merge stay bitwise equal.
 """
 import numpy as np
 import pytest
+import torch
 
 import paged_fp8_kv_gqa_gb300 as xqa
 from gpu_helpers import Dev, assert_close, oracle_of, run, to_dev
+from oracle import plan as oplan
 from paged_fp8_kv_gqa_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
+
+MIN_PIECES, MAX_PIECE_PAGES = 4, 32  # the kernel's warp-mode rule
+
+
+def _warp_mode_share(w):
+    """Share of the non-empty CTA ranges that meet the warp-mode rule (0 when
+    the host does not pick the warp-mode kernel): at least MIN_PIECES pieces,
+    none longer than MAX_PIECE_PAGES pages. Computed from the oracle's plan, to
+    show that a test batch really exercises the mode."""
+    n_max = torch.cuda.get_device_properties(0).multi_processor_count
+    hkv = w.num_kv_heads
+    if w.batch * hkv < MIN_PIECES * n_max:
+        return 0.0
+    pl = oplan.plan(w.context_lens, hkv, w.block_tables.shape[1], n_max, 16)
+    st, cc, n = pl["seg_start"], pl["seg_cc"], pl["num_ctas"]
+    hits = ranges = 0
+    for i in range(n):
+        a, e = oplan.cta_range(i, st, cc, n)
+        if a == e:
+            continue
+        ranges += 1
+        s = int(np.searchsorted(st, a, side="right") - 1)
+        lens = []
+        while s < len(st) - 1 and st[s] < e:
+            lens.append(int(min(st[s + 1], e) - max(st[s], a)))
+            s += 1
+        if sum(x > 0 for x in lens) >= MIN_PIECES and max(lens) <= MAX_PIECE_PAGES:
+            hits += 1
+    return hits / ranges
 
 
 def _short_batch(seed, hq=32, hkv=4, q_len=1, kv_dtype="e5m2", batch=160):
@@ -31,6 +62,7 @@ def _short_batch(seed, hq=32, hkv=4, q_len=1, kv_dtype="e5m2", batch=160):
 @pytest.mark.parametrize("hq,hkv,q_len", [(32, 4, 1), (16, 4, 2), (8, 8, 1)])
 def test_warp_mode_matches_oracle(kv_dtype, hq, hkv, q_len):
     w = _short_batch(101 + hq + q_len, hq, hkv, q_len, kv_dtype, batch=160 if hkv == 4 else 80)
+    assert _warp_mode_share(w) > 0.5  # most ranges in warp mode, the rest in CTA mode
     a = run(w, merge_mode=0)
     b = run(w, merge_mode=1)
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
