@@ -7,7 +7,7 @@ The page "[Kernel][WIP] Follow up FlashNext batch HC fusion and QSA route audit"
 merge, and records that a capacity-sized grid leaves CTAs empty on short
 contexts while fixed grids or contiguous grouping regress long contexts, and
 that too few CTAs is catastrophic. The pages give no partition rule; the one
-this build adopts (a reading) sizes every split from the total work:
+adopted here (a reading) sizes every split from the total work:
 
 * a *segment* is one (sequence b, kv head g) pair, index ``s = b*Hkv + g``; it
   holds ``ceil(ctx_b / BS)`` pages (0 if ``ctx_b`` is 0 or invalid);

@@ -3,11 +3,12 @@
 // One persistent CTA per planner share of the flattened (sequence, kv head,
 // page) order, cut on the planner's cost line (each segment's switch cost
 // counted beside its pages; the CTA derives the plan itself from the context
-// lengths when the segment table fits in shared memory). Its phases are the
-// ones profiled on the page "[Kernel][SM70]
-// Pipeline batched E5M2 XQA decode" (section "Pending work and gates"): K load +
-// E5M2 conversion, shared-memory publication, QK, V load + conversion, PV and
-// synchronization. That page's starting kernel was memory-latency bound
+// lengths when the segment table fits in shared memory). Its steps are the
+// phases whose cost the page "[Kernel][SM70] Pipeline batched E5M2 XQA decode"
+// (section "Pending work and gates") sets out to attribute: bringing in K and
+// decoding it from E5M2, making it visible to the other warps through shared
+// memory, the QK product, bringing in and decoding V, the PV product, and the
+// waits between them. That page's starting kernel was memory-latency bound
 // (long-scoreboard stalls at low occupancy, section "Starting bottleneck"); on
 // sm_103a this kernel keeps kStages pages in flight per SM instead.
 //

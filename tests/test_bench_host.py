@@ -1,0 +1,61 @@
+"""Host-side helpers of bench.py (no GPU): the clock summary, quantiles, the
+code hash that decides whether the committed ncu traffic still applies, and
+the committed profile summary's machine-read lines."""
+import os
+import re
+
+import numpy as np
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_code_only_drops_comments_and_keeps_literals():
+    src = ('int a = 1;  // note\n/* block\n   comment */ const char* s = "// kept";\n'
+           "char q = '\"'; asm(\"mov.b32 %0, %1; // in a string\");\n")
+    out = bench._code_only(src)
+    assert "note" not in out and "block" not in out
+    assert '"// kept"' in out and "'\"'" in out and "// in a string" in out
+    assert out == bench._code_only(src.replace("  // note", "  // another note"))
+    assert out != bench._code_only(src.replace("a = 1", "a = 2"))
+
+
+def test_kernel_hash_ignores_comment_edits_only():
+    path = os.path.join(ROOT, bench.KERNEL_SOURCES[0])
+    text = open(path, encoding="utf-8").read()
+    base = bench._code_only(text)
+    assert bench._code_only(text.replace("// ", "//  edited ", 5)) == base
+    assert "__launch_bounds__(kThreads, 1)" in text
+    changed = text.replace("__launch_bounds__(kThreads, 1)", "__launch_bounds__(kThreads, 2)", 1)
+    assert bench._code_only(changed) != base
+
+
+def test_profile_summary_lines_parse_and_match_the_kv_bytes():
+    text = open(bench.PROFILE_SUMMARY).read()
+    src = re.search(r"^kernel_source_sha256: ([0-9a-f]{16})$", text, re.M)
+    traffic = re.search(r"^dram_bytes_per_launch: (\d+)$", text, re.M)
+    assert src and traffic
+    kv_bytes = 286_227_456  # sum of B16 ragged contexts x 4 kv heads x 256 B
+    # DRAM traffic of one launch: every KV byte once, plus q, tables and outputs
+    assert kv_bytes <= int(traffic.group(1)) <= 1.02 * kv_bytes
+
+
+def test_summarize_clocks_median_max_and_reasons():
+    rows = [
+        ["0", "2070", "2070", "900", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"],
+        ["0", "1980", "2070", "1100", "0x4", "Not Active", "Not Active", "Not Active", "Active"],
+        ["0", "2070", "2070", "1000", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"],
+        ["0", "[N/A]", "2070", "1000", "0x0", "", "", "", ""],
+    ]
+    c = bench.summarize_clocks(rows)
+    assert c == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    assert bench.summarize_clocks([]) is None
+
+
+def test_quantile_matches_numpy_linear():
+    rng = np.random.default_rng(3)
+    for n in (1, 2, 5, 17):
+        v = sorted(rng.normal(size=n).tolist())
+        for q in (0.0, 0.1, 0.5, 0.9, 1.0):
+            assert abs(bench._quantile(v, q) - np.quantile(v, q)) < 1e-12
