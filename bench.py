@@ -586,7 +586,16 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "kv_bytes_per_step": bytes_per_step},
+        "config": {
+            "workload": args.workload,
+            "batch": w.batch, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size,
+            "total_context_tokens": int(w.context_lens.sum()),
+            "kv_bytes_per_step": int(w.context_lens.sum()) * w.num_kv_heads * w.head_dim * 2,
+            "sample_kv_bytes_per_step": bytes_per_step,
+            "kv_dtype": w.kv_dtype, "kv_layout": w.kv_layout, "q_len": 1,
+            "parallelism": "single process (rank 0)",
+        },
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": _threads_note(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
