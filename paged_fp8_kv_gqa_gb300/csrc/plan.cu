@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             int min_pages, int32_t* ws) {
   griddep_wait();               // everything earlier on the stream is complete
   griddep_launch_dependents();  // the partial kernel may start its prologue now
+  constexpr int kPlanWarps = kPlanThreads / 32;
   const int nseg = batch * num_kv_heads;
   const WsLayout lay = ws_layout(nseg, 0);
   int32_t* header = ws;
@@ -47,60 +48,61 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   int32_t* seg_bad = ws + lay.seg_bad_off / 4;
   int32_t* seg_count = ws + lay.seg_count_off / 4;
   int32_t* seg_cc = ws + lay.seg_cc_off / 4;
-  __shared__ int warp_total[kPlanThreads / 32], warp_cost[kPlanThreads / 32];
-  __shared__ int carry, carry_cost;
+  __shared__ int warp_total[kPlanWarps], warp_cost[kPlanWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    header[0] = XQA_OK;
-    carry = 0;
-    carry_cost = 0;
+  if (tid == 0) header[0] = XQA_OK;
+  __syncthreads();  // the reset comes before any thread records an error
+  const long long max_ctx = (long long)max_blocks_per_seq * kBlockSize;
+  auto pages_of = [&](int s, bool& bad) {
+    const int ctx = context_lens[s / num_kv_heads];
+    bad = ctx < 0 || (long long)ctx > max_ctx;
+    return bad ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
+  };
+  // Thread tid owns the consecutive segments [s0, s1). Its pages and costs
+  // are summed first (independent loads, no stores in between), one block
+  // scan turns the sums into the thread's offsets, and a second pass writes
+  // the rows: one scan and a single round of load latency for any batch.
+  const int per = (nseg + kPlanThreads - 1) / kPlanThreads;
+  const int s0 = min(nseg, tid * per), s1 = min(nseg, s0 + per);
+  int my_pages = 0, my_cost = 0;
+#pragma unroll 8
+  for (int s = s0; s < s1; ++s) {
+    bool bad;
+    const int pg = pages_of(s, bad);
+    my_pages += pg;
+    my_cost += seg_cost(pg);
+  }
+  const int incl = warp_inclusive_scan(my_pages);
+  const int incl_cost = warp_inclusive_scan(my_cost);
+  if (lane == 31) {
+    warp_total[warp] = incl;
+    warp_cost[warp] = incl_cost;
   }
   __syncthreads();
-  const long long max_ctx = (long long)max_blocks_per_seq * kBlockSize;
-  for (int base = 0; base < nseg; base += kPlanThreads) {
-    const int s = base + tid;
-    int pages = 0;
-    if (s < nseg) {
-      const int ctx = context_lens[s / num_kv_heads];
-      const bool bad = ctx < 0 || (long long)ctx > max_ctx;
-      if (bad) record_status(&header[0], XQA_ERR_CTX_TOO_LONG);
-      pages = bad ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
-      seg_bad[s] = bad ? 1 : 0;
-      seg_count[s] = 0;
+  if (warp == 0) {
+    const int t = warp_inclusive_scan(lane < kPlanWarps ? warp_total[lane] : 0);
+    const int tc = warp_inclusive_scan(lane < kPlanWarps ? warp_cost[lane] : 0);
+    if (lane < kPlanWarps) {
+      warp_total[lane] = t;
+      warp_cost[lane] = tc;
     }
-    const int cost = seg_cost(pages);
-    const int incl = warp_inclusive_scan(pages);
-    const int incl_cost = warp_inclusive_scan(cost);
-    if (lane == 31) {
-      warp_total[warp] = incl;
-      warp_cost[warp] = incl_cost;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      constexpr int kPlanWarps = kPlanThreads / 32;
-      const int t = warp_inclusive_scan(lane < kPlanWarps ? warp_total[lane] : 0);
-      const int tc = warp_inclusive_scan(lane < kPlanWarps ? warp_cost[lane] : 0);
-      if (lane < kPlanWarps) {
-        warp_total[lane] = t;
-        warp_cost[lane] = tc;
-      }
-    }
-    __syncthreads();
-    const int excl = carry + incl - pages + (warp > 0 ? warp_total[warp - 1] : 0);
-    const int cc = carry_cost + incl_cost + (warp > 0 ? warp_cost[warp - 1] : 0);
-    if (s < nseg) {
-      seg_start[s] = excl;
-      seg_cc[s] = cc;
-    }
-    __syncthreads();
-    if (tid == kPlanThreads - 1) {
-      carry = excl + pages;
-      carry_cost = cc;
-    }
-    __syncthreads();
   }
-  if (tid == 0) {
-    const int total = carry;
+  __syncthreads();
+  int start = incl - my_pages + (warp > 0 ? warp_total[warp - 1] : 0);  // exclusive
+  int cc = incl_cost - my_cost + (warp > 0 ? warp_cost[warp - 1] : 0);
+  for (int s = s0; s < s1; ++s) {
+    bool bad;
+    const int pg = pages_of(s, bad);
+    if (bad) record_status(&header[0], XQA_ERR_CTX_TOO_LONG);
+    seg_bad[s] = bad ? 1 : 0;
+    seg_count[s] = 0;
+    seg_start[s] = start;
+    cc += seg_cost(pg);
+    seg_cc[s] = cc;  // inclusive: the switch costs of segments 0 .. s
+    start += pg;
+  }
+  if (tid == kPlanThreads - 1) {
+    const int total = warp_total[kPlanWarps - 1];
     seg_start[nseg] = total;
     header[2] = total;
     header[3] = nseg;
