@@ -53,7 +53,11 @@ constexpr int kSegCost = 32;
 // pieces, none longer than kWarpModePages pages, gives whole pieces to warps.
 constexpr int kWarpModeMinPieces = 4;
 constexpr int kWarpModePages = 32;
-constexpr int kPlanThreads = 256;  // small enough to share an SM with a partial CTA
+// The planner is one CTA. Its registers do not fit beside a partial CTA (which
+// takes 61,440 of the SM's 65,536), so the partial CTA bound for the
+// planner's SM starts when the planner exits; the planner therefore does one
+// scan and a single round of loads whatever the batch.
+constexpr int kPlanThreads = 256;
 constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
 
 // Partial-result slot: O[col][128] unnormalised fp32, then M[col] (log2 domain),
