@@ -4,12 +4,13 @@
  *
  * One decode step: every sequence b contributes one query token with Hq heads;
  * its keys and values live in a paged FP8 E5M2 cache; q head h attends over the
- * ctx_b cached tokens of kv head h / G (G = Hq / Hkv). This is the batched,
- * long-context XQA decode on an E5M2 KV cache of the page "[Kernel][SM70]
- * Pipeline batched E5M2 XQA decode" (sections "Purpose" and "Starting
- * bottleneck"), whose phases (K load + E5M2 conversion, shared-memory
- * publication, QK, V load + conversion, PV, synchronization; section "Pending
- * work and gates") are the steps of the partial kernel below. The split-KV
+ * ctx_b cached tokens of kv head h / G (G = Hq / Hkv). This is the operation
+ * the page "[Kernel][SM70] Pipeline batched E5M2 XQA decode" optimises: one
+ * step for many long sequences at once, keys and values stored as E5M2
+ * (sections "Purpose" and "Starting bottleneck"). The partial kernel below is built from the phases that page
+ * times separately (section "Pending work and gates"): fetching and decoding
+ * K, sharing it through shared memory, QK, fetching and decoding V, PV, and
+ * the synchronisation between them. The split-KV
  * planner -> forward -> merge structure follows the page "[Kernel][WIP] Follow
  * up FlashNext batch HC fusion and QSA route audit" (section "Test Result").
  *
@@ -195,7 +196,7 @@ xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int3
 
 /* xqa_decode for callers that cannot allocate device memory.
  *
- * The paper has no counterpart to this entry point. It exists for callers that
+ * None of the pages describes this entry point. It exists for callers that
  * are not allowed to call cudaMalloc: a plugin inside a host runtime that owns
  * all device memory through its own pool, a latency-critical path where an
  * allocation (which may synchronise the device) is forbidden, or an operator

@@ -4,8 +4,9 @@ Test infrastructure only (see the package docstring).
 
 What it computes is the plain definition of one decode step of grouped-query
 attention (page "[Kernel][SM70] Pipeline batched E5M2 XQA decode", section
-"Purpose": batched long-context XQA decode on an FP8 E5M2 KV cache; section
-"Pending work and gates": randomized-page operator checks, boundary contexts).
+"Purpose": decoding many long sequences at once over an FP8 E5M2 KV cache;
+section "Pending work and gates": checks with pages placed at random and with
+edge-case context lengths).
 The pages print no formula, so the following readings are taken:
 
 * q head ``h`` reads kv head ``h // G`` with ``G = Hq / Hkv`` (consecutive groups);

@@ -2,9 +2,10 @@
 
 Tolerance: every fp16 output element must satisfy |gpu - ref| <= 2e-3 + 1e-2*|ref|
 (ref = unrounded float64 oracle). Plus bitwise properties: page relocation
-invariance and poisoned-memory invariance (the "bitwise randomized-page operator
-A/B" and boundary-context gates on the page "[Kernel][SM70] Pipeline batched E5M2
-XQA decode", section "Pending work and gates"), CUDA-graph replay with changed
+invariance and poisoned-memory invariance (the page "[Kernel][SM70] Pipeline
+batched E5M2 XQA decode", section "Pending work and gates", gates its kernel on
+bit-identical output when pages are placed at random, and on edge-case context
+lengths), CUDA-graph replay with changed
 inputs (the changed-input graph replays on the page "[Kernel][WIP] Follow up
 FlashNext batch HC fusion and QSA route audit", section "Test Result"),
 determinism, and the device-side error paths.

@@ -9,8 +9,8 @@ Each pin ties the float64 oracle to something other than itself:
 * torch's scaled_dot_product_attention in float64 on KV gathered by loops here;
 * GQA head mapping and masking, with poisoned pages and tail slots;
 * page permutation: relocating pages leaves the output bitwise unchanged (the
-  "bitwise randomized-page operator A/B" gate on the page "[Kernel][SM70]
-  Pipeline batched E5M2 XQA decode", section "Pending work and gates").
+  page "[Kernel][SM70] Pipeline batched E5M2 XQA decode", section "Pending work
+  and gates", requires bit-identical results under random page placement).
 
 The mutation tests at the end plant plausible mistakes in the oracle's own
 source (a dropped scale, a transposed head mapping, an off-by-one gather, ...)
