@@ -81,3 +81,43 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(xqa, "LIB_PATH", "/nonexistent/libxqa.so")
     with pytest.raises(RuntimeError, match="missing"):
         xqa.load_library()
+
+
+def test_argument_checks_come_before_any_device_call(lib):
+    # Addresses below are never dereferenced: each call is rejected by a host
+    # check that runs before the first CUDA call (max_ctas is explicit, so no
+    # SM-count query either). Pointer order: q, K, V, tables, lengths, out.
+    shape = xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0)
+    n = ctypes.c_size_t(0)
+    assert lib.xqa_workspace_size(ctypes.byref(shape), ctypes.byref(n)) == xqa.XQA_OK
+    q, k, v, bt, lens, out, ws = (0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000,
+                                  0x100000)
+    sh = ctypes.byref(shape)
+
+    def decode(q, k, v, bt, lens, out, ws=ws, nbytes=n.value):
+        return lib.xqa_decode(q, k, v, bt, lens, 1.0, 1.0, out, sh, ws, nbytes, None)
+
+    assert decode(q, k, v, bt, lens, out, ws=ws + 128) == xqa.XQA_ERR_ALIGN  # 256-B workspace
+    assert decode(q, k, v, bt, lens, out, ws=0) == xqa.XQA_ERR_NULL
+    assert decode(q, k, v, bt, lens, out, nbytes=n.value - 1) == xqa.XQA_ERR_WORKSPACE
+    for i in (0, 1, 2, 5):  # q, K, V and out must be 16-byte aligned
+        ptrs = [q, k, v, bt, lens, out]
+        ptrs[i] += 8
+        assert decode(*ptrs) == xqa.XQA_ERR_ALIGN, i
+    assert lib.xqa_attend_partial(q + 2, k, v, bt, lens, 1.0, 1.0, out, sh, ws, n.value,
+                                  None) == xqa.XQA_ERR_ALIGN
+    assert lib.xqa_plan(None, sh, ws, n.value, None) == xqa.XQA_ERR_NULL
+    assert lib.xqa_plan(lens, sh, ws + 16, n.value, None) == xqa.XQA_ERR_ALIGN
+    assert lib.xqa_plan(lens, sh, ws, 64, None) == xqa.XQA_ERR_WORKSPACE
+    assert lib.xqa_combine(lens, 1.0, out + 2, sh, ws, n.value, None) == xqa.XQA_ERR_ALIGN
+    negative = xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, -1, 0)
+    assert lib.xqa_decode(q, k, v, bt, lens, 1.0, 1.0, out, ctypes.byref(negative), ws, n.value,
+                          None) == xqa.XQA_ERR_SHAPE
+    # the static-workspace entry point rejects a shape its array cannot hold
+    m = re.search(r"#define XQA_STATIC_WORKSPACE_BYTES \(\(size_t\)(\d+) << (\d+)\)",
+                  open(HEADER).read())
+    static_bytes = int(m.group(1)) << int(m.group(2))
+    big = xqa.XqaShape(8192, 32, 4, 128, 16, 16, 16, 0.0, 152, 0)
+    assert xqa.xqa_workspace_size(big) > static_bytes
+    assert lib.xqa_decode_static_workspace(q, k, v, bt, lens, 1.0, 1.0, out, ctypes.byref(big),
+                                           None) == xqa.XQA_ERR_WORKSPACE
