@@ -93,6 +93,10 @@ typedef struct xqa_shape {
  * device (depends on the SM count when max_ctas == 0). Host only. */
 xqa_status_t xqa_workspace_size(const xqa_shape_t* shape, size_t* bytes);
 
+/* Number of kernels one xqa_decode call enqueues for `shape` (so a caller can
+ * size CUDA graphs or count launches). Host only; *kernels receives 1, 2 or 3. */
+xqa_status_t xqa_kernels_per_call(const xqa_shape_t* shape, int32_t* kernels);
+
 /* One decode step of paged GQA attention.
  *
  *   q             device, fp16 [B, Hq, D] ([B, T, Hq, D] with q_len T > 1),

@@ -9,7 +9,7 @@ The names mirror the C ABI declared in ``include/xqa.h``:
 ``xqa_workspace_size``, ``xqa_decode``, ``xqa_plan``, ``xqa_attend_partial``,
 ``xqa_combine``, ``xqa_decode_device_scales``, ``xqa_dequant_e5m2``,
 ``xqa_dequant_e4m3``, ``xqa_read_status``, ``xqa_read_plan``, ``xqa_status_string``,
-``xqa_decode_static_workspace``.
+``xqa_decode_static_workspace``, ``xqa_kernels_per_call``.
 """
 from __future__ import annotations
 
@@ -46,6 +46,7 @@ EXPORTED = (
     "xqa_decode_device_scales",
     "xqa_dequant_e4m3",
     "xqa_selftest_wait_timeout",
+    "xqa_kernels_per_call",
 )
 
 KV_DTYPES = {"e5m2": 0, "e4m3": 1}
@@ -99,6 +100,7 @@ _SIGS = {
     "xqa_decode_device_scales": [_P, _P, _P, _P, _P, _P, _P, _P, _SHAPE, _P, _SZ, _P],
     "xqa_dequant_e4m3": [_P, _SZ, _F, _P, _P, _P],
     "xqa_selftest_wait_timeout": [_P, ctypes.c_uint64, _P],
+    "xqa_kernels_per_call": [_SHAPE, ctypes.POINTER(ctypes.c_int32)],
 }
 
 
@@ -170,6 +172,14 @@ def xqa_workspace_size(shape: XqaShape) -> int:
     n = _SZ(0)
     _check(load_library().xqa_workspace_size(ctypes.byref(shape), ctypes.byref(n)),
            "xqa_workspace_size")
+    return int(n.value)
+
+
+def xqa_kernels_per_call(shape: XqaShape) -> int:
+    """Kernels one xqa_decode call enqueues for this shape."""
+    n = ctypes.c_int32(0)
+    _check(load_library().xqa_kernels_per_call(ctypes.byref(shape), ctypes.byref(n)),
+           "xqa_kernels_per_call")
     return int(n.value)
 
 

@@ -155,6 +155,15 @@ xqa_status_t xqa_workspace_size(const xqa_shape_t* shape, size_t* bytes) {
   return XQA_OK;
 }
 
+xqa_status_t xqa_kernels_per_call(const xqa_shape_t* shape, int32_t* kernels) {
+  if (!kernels) return XQA_ERR_NULL;
+  Resolved r;
+  xqa_status_t st = resolve(shape, &r);
+  if (st != XQA_OK) return st;
+  *kernels = 2 + (r.merge_mode == 1 ? 1 : 0);  // planner, partial (+ combine)
+  return XQA_OK;
+}
+
 xqa_status_t xqa_plan(const int32_t* context_lens, const xqa_shape_t* shape, void* workspace,
                       size_t workspace_bytes, void* stream) {
   if (!context_lens) return XQA_ERR_NULL;
