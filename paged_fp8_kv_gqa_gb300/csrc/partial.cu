@@ -465,60 +465,87 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
   }
 }
 
-}  // namespace
+// ---------------------------------------------------------------------------
+// The parts of a partial CTA's work that both kernels below share.
+// ---------------------------------------------------------------------------
 
-template <int kFmt, int NT, bool kMulti>
-__global__ void __launch_bounds__(kThreads, 1)
-    partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const PartialParams p) {
-  using Geom = PartialGeom<NT>;
-  constexpr int kCols = Geom::kCols;
-  constexpr int kBufs = Geom::kMergeBufs;
-  constexpr bool kPairs = true;  // two pages per warp iteration
-  constexpr bool kPrefetchQ = NT == 1;  // registers: two-tile kernels load Q per segment
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kStages];
-  __shared__ int stage_bad[kStages];
-  __shared__ int abort_flag;
-
-  __shared__ int scan_warp[kWarps], scan_warp_cost[kWarps];
-  __shared__ int scan_carry, scan_carry_cost;
-  __shared__ long long cost_line;  // kept here: the end of the kernel reads it back
-  __shared__ int range_lo, range_hi, range_seg, range_seg_hi;  // pages; first, last segment
-  __shared__ const int32_t* cc_base;  // the cost-line prefix the end of the kernel reads
+// Static shared state of one partial CTA (the ring, the merge buffers and the
+// segment caches live in dynamic shared memory).
+template <int NT>
+struct CtaShared {
+  static constexpr int kBufs = PartialGeom<NT>::kMergeBufs;
+  uint64_t full_bar[kStages];  // one per ring slot: the slot's K and V pages landed
+  int stage_bad[kStages];      // the slot's page had a block id outside [0, NB)
+  int abort_flag;              // a wait ran out of time: stop issuing, drain
+  int scan_warp[kWarps], scan_warp_cost[kWarps];
+  int scan_carry, scan_carry_cost;
+  long long cost_line;  // kept here: the end of the kernel reads it back
+  int range_lo, range_hi, range_seg, range_seg_hi;  // pages; first, last segment
+  const int32_t* cc_base;  // the cost-line prefix the end of the kernel reads
   // split pieces of this CTA (at most its first and last segment), whose
   // merge tickets are taken once the whole range is done
-  __shared__ int pend_seg[2], pend_poison[2], pend_last[2];
-  __shared__ int npend;
+  int pend_seg[2], pend_poison[2], pend_last[2];
+  int npend;
   // the segment each merge buffer holds, whether this CTA owns it whole, and
   // each warp's "met a bad page" flag for it
-  __shared__ int buf_seg[kBufs], buf_whole[kBufs], buf_poison[kBufs][kWarps];
+  int buf_seg[kBufs], buf_whole[kBufs], buf_poison[kBufs][kWarps];
+};
 
+// Dynamic shared memory of a partial CTA: the 1024-byte aligned ring of
+// kStages (K, V) page slots, then the merge buffers and the three segment
+// caches (segment starts, context lengths, cost-line prefix).
+template <int NT>
+struct CtaSmem {
+  uint8_t* stages;
+  float* merge_bufs;
+  int32_t* seg_cache;
+  int32_t* ctx_cache;
+  int32_t* cc_cache;
+};
+
+template <int NT>
+__device__ __forceinline__ CtaSmem<NT> carve_smem(uint8_t* smem_raw) {
+  CtaSmem<NT> m;
+  m.stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  m.merge_bufs = reinterpret_cast<float*>(m.stages + kStages * kStageBytes);
+  m.seg_cache = reinterpret_cast<int32_t*>(m.merge_bufs +
+                                           PartialGeom<NT>::kMergeBufs * PartialGeom<NT>::kMergeBufFloats);
+  m.ctx_cache = m.seg_cache + kSegCache;  // context length per sequence
+  m.cc_cache = m.ctx_cache + kSegCache;   // cost-line prefix per segment
+  return m;
+}
+
+// This CTA's range of the flattened (segment, page) order and the tables it
+// reads them through. segs / cc / ctxs index by global segment (sequence)
+// number even when they point into a shared window of the tables.
+struct RangeView {
+  const int32_t* segs;  // segment starts
+  const int32_t* cc;    // cost-line prefix
+  const int32_t* ctxs;  // context lengths
+  int total, n;         // pages of the step, CTAs that hold work
+  int cbeg, cend, npages;
+  int s_first, s_hi;  // the range's first segment, the last any lookup can reach
+};
+
+// The plan (computed here when the segment table fits in shared memory, with
+// the same integer rule as the planner kernel, else read from the planner),
+// the rows of empty segments, and this CTA's range on the cost line. Also
+// initialises the ring barriers. Returns false when this CTA holds no page.
+template <int NT>
+__device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtensorMap* tm_k,
+                                            const CUtensorMap* tm_v, CtaShared<NT>& sh,
+                                            const CtaSmem<NT>& sm, RangeView& rv) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
-  griddep_launch_dependents();  // a dependent next kernel waits for this grid itself
   const int nseg = p.batch * p.num_kv_heads;
   const int ncols = p.group * p.q_len;
-  // per-tensor scales: host values, or device scalars read when the kernel runs
-  const float k_scale = p.k_scale_ptr ? __ldg(p.k_scale_ptr) : p.k_scale;
-  const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
-  const float scale_log2 = static_cast<float>(p.qk_scale_base * static_cast<double>(k_scale));
-
-  uint8_t* stages = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* merge_bufs = reinterpret_cast<float*>(stages + kStages * kStageBytes);
-  int32_t* seg_cache = reinterpret_cast<int32_t*>(merge_bufs + kBufs * Geom::kMergeBufFloats);
-  int32_t* ctx_cache = seg_cache + kSegCache;  // context length per sequence
-  int32_t* cc_cache = ctx_cache + kSegCache;   // cost-line prefix per segment
-
-  // ---- the plan: computed here when the segment table fits in shared memory
-  // (same integer rule as the planner kernel), else read from the planner ----
   const bool segs_in_smem = nseg + 1 <= kSegCache;
   const int32_t* segs;
   const int32_t* cc;
   int total, n;
   if (segs_in_smem) {
-    if (tid == 0) scan_carry = scan_carry_cost = 0;
+    if (tid == 0) sh.scan_carry = sh.scan_carry_cost = 0;
     __syncthreads();
     const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
     for (int base = 0; base < p.batch; base += kThreads) {
@@ -526,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pages = 0;
       if (b < p.batch) {
         const int ctx = __ldg(&p.context_lens[b]);
-        ctx_cache[b] = ctx;
+        sm.ctx_cache[b] = ctx;
         pages = (ctx < 0 || (long long)ctx > max_ctx) ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
       }
       const int cost = seg_cost(pages);  // every kv head's segment of sequence b
@@ -541,34 +568,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (lane == 31) {
-        scan_warp[warp] = incl;
-        scan_warp_cost[warp] = incl_cost;
+        sh.scan_warp[warp] = incl;
+        sh.scan_warp_cost[warp] = incl_cost;
       }
       __syncthreads();
-      int before = scan_carry, before_cost = scan_carry_cost;
+      int before = sh.scan_carry, before_cost = sh.scan_carry_cost;
       for (int w = 0; w < warp; ++w) {
-        before += scan_warp[w];
-        before_cost += scan_warp_cost[w];
+        before += sh.scan_warp[w];
+        before_cost += sh.scan_warp_cost[w];
       }
       const int excl = before + incl - pages;
       const int excl_cost = before_cost + incl_cost - cost;
       if (b < p.batch)
         for (int h = 0; h < p.num_kv_heads; ++h) {
-          seg_cache[b * p.num_kv_heads + h] = excl * p.num_kv_heads + h * pages;
-          cc_cache[b * p.num_kv_heads + h] = excl_cost * p.num_kv_heads + (h + 1) * cost;
+          sm.seg_cache[b * p.num_kv_heads + h] = excl * p.num_kv_heads + h * pages;
+          sm.cc_cache[b * p.num_kv_heads + h] = excl_cost * p.num_kv_heads + (h + 1) * cost;
         }
       __syncthreads();
       if (tid == kThreads - 1) {
-        scan_carry = excl + pages;
-        scan_carry_cost = excl_cost + cost;
+        sh.scan_carry = excl + pages;
+        sh.scan_carry_cost = excl_cost + cost;
       }
       __syncthreads();
     }
-    total = scan_carry * p.num_kv_heads;
-    if (tid == 0) seg_cache[nseg] = total;
+    total = sh.scan_carry * p.num_kv_heads;
+    if (tid == 0) sm.seg_cache[nseg] = total;
     n = num_ctas_for(total, p.n_max, p.min_pages);
-    segs = seg_cache;
-    cc = cc_cache;
+    segs = sm.seg_cache;
+    cc = sm.cc_cache;
   } else {
     griddep_wait();
     total = p.header[2];
@@ -595,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (cta >= n) return;
+  if (cta >= n) return false;
   // This CTA's positions [vlo, vhi) on the cost line, and the pages there: the
   // first page at a position >= a lies in the first segment whose pages end
   // past a. One parallel pass over the segments finds both ends (and the
@@ -603,15 +630,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long line = (long long)total + (nseg > 0 ? cc[nseg - 1] : 0);
   const long long vlo = ((long long)cta * line) / n, vhi = ((long long)(cta + 1) * line) / n;
   if (tid == 0) {
-    cost_line = line;
-    range_lo = range_hi = total;  // no segment ends past the position
-    range_seg = nseg;
-    range_seg_hi = nseg - 1;
-    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
-    abort_flag = 0;
+    sh.cost_line = line;
+    sh.range_lo = sh.range_hi = total;  // no segment ends past the position
+    sh.range_seg = nseg;
+    sh.range_seg_hi = nseg - 1;
+    for (int i = 0; i < kStages; ++i) mbar_init(&sh.full_bar[i], 1);
+    sh.abort_flag = 0;
+    sh.npend = 0;
     fence_mbar_init();
-    prefetch_tensormap(&tm_k);
-    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(tm_k);
+    prefetch_tensormap(tm_v);
   }
   __syncthreads();
   for (int s = tid; s < nseg; s += kThreads) {
@@ -619,52 +647,245 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long prev = s > 0 ? (long long)segs[s] + cc[s - 1] : -1;  // previous one's end
     const long long first = (long long)segs[s] + cc[s];                   // its first page
     if (end > vlo && prev <= vlo) {
-      range_lo = vlo <= first ? segs[s] : (int)(segs[s] + (vlo - first));
-      range_seg = s;
+      sh.range_lo = vlo <= first ? segs[s] : (int)(segs[s] + (vlo - first));
+      sh.range_seg = s;
     }
     if (end > vhi && prev <= vhi) {
-      range_hi = vhi <= first ? segs[s] : (int)(segs[s] + (vhi - first));
-      range_seg_hi = s;  // the range's last segment is this one or an earlier one
+      sh.range_hi = vhi <= first ? segs[s] : (int)(segs[s] + (vhi - first));
+      sh.range_seg_hi = s;  // the range's last segment is this one or an earlier one
     }
   }
   __syncthreads();
-  const int cbeg = range_lo, cend = range_hi;
-  const int npages = cend - cbeg;
-  if (npages <= 0) return;  // its share of the line is segment switch cost only
-  const int s_first = range_seg;
+  rv.cbeg = sh.range_lo;
+  rv.cend = sh.range_hi;
+  rv.npages = rv.cend - rv.cbeg;
+  if (rv.npages <= 0) return false;  // its share of the line is segment switch cost only
+  rv.s_first = sh.range_seg;
+  rv.total = total;
+  rv.n = n;
   // With the planner's table in global memory, the few segments this range
   // touches (a contiguous run) are copied into the shared caches, and the
   // table pointers are shifted so that segment s still reads entry s.
-  int s_hi = nseg - 1;  // the last segment any lookup of this range can reach
-  const int32_t* ctxs = segs_in_smem ? ctx_cache : p.context_lens;
+  rv.s_hi = nseg - 1;
+  rv.ctxs = segs_in_smem ? sm.ctx_cache : p.context_lens;
   if (!segs_in_smem) {
-    const int wn = range_seg_hi - s_first + 1;
+    const int s_first = rv.s_first;
+    const int wn = sh.range_seg_hi - s_first + 1;
     const int b_first = s_first / p.num_kv_heads;
-    const int wb = range_seg_hi / p.num_kv_heads - b_first + 1;
+    const int wb = sh.range_seg_hi / p.num_kv_heads - b_first + 1;
     if (wn + 1 <= kSegCache && wb <= kSegCache) {
       for (int i = tid; i <= wn; i += kThreads) {
-        seg_cache[i] = segs[s_first + i];
-        if (i < wn) cc_cache[i] = cc[s_first + i];
+        sm.seg_cache[i] = segs[s_first + i];
+        if (i < wn) sm.cc_cache[i] = cc[s_first + i];
       }
-      for (int i = tid; i < wb; i += kThreads) ctx_cache[i] = __ldg(&p.context_lens[b_first + i]);
+      for (int i = tid; i < wb; i += kThreads) sm.ctx_cache[i] = __ldg(&p.context_lens[b_first + i]);
       __syncthreads();
-      segs = seg_cache - s_first;
-      cc = cc_cache - s_first;
-      ctxs = ctx_cache - b_first;
-      s_hi = range_seg_hi;
+      segs = sm.seg_cache - s_first;
+      cc = sm.cc_cache - s_first;
+      rv.ctxs = sm.ctx_cache - b_first;
+      rv.s_hi = sh.range_seg_hi;
     }
   }
-  if (tid == 0) cc_base = cc;
-  volatile int* abort = &abort_flag;
-  const uint64_t policy = l2_evict_first_policy();
+  rv.segs = segs;
+  rv.cc = cc;
+  if (tid == 0) sh.cc_base = cc;
+  return true;
+}
+
+// Lane 0 of a warp: the two TMA loads (K and V slice of one page) into ring
+// slot `slot`, completing on its barrier; a page with a bad block id is
+// flagged instead (the slot's barrier completes without data).
+template <int NT>
+__device__ __forceinline__ void issue_page(const PartialParams& p, const CUtensorMap* tm_k,
+                                           const CUtensorMap* tm_v, CtaShared<NT>& sh,
+                                           uint8_t* stages, int slot, int y, int bad, int sg,
+                                           uint64_t policy) {
+  uint8_t* st = stages + slot * kStageBytes;
+  sh.stage_bad[slot] = bad;
+  fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
+  if (bad) {
+    griddep_wait();  // the planner resets seg_bad and the status word
+    atomicOr(&p.seg_bad[sg], 1);
+    record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
+    mbar_arrive(&sh.full_bar[slot]);
+  } else {
+    mbar_arrive_expect_tx(&sh.full_bar[slot], kStageBytes);
+    if (p.kv_layout == XQA_LAYOUT_HND) {
+      tma_load_2d(st, tm_k, &sh.full_bar[slot], 0, y, policy);
+      tma_load_2d(st + kPageBytes, tm_v, &sh.full_bar[slot], 0, y, policy);
+    } else {  // NHD: box (128 dims, 1 kv head, 16 tokens) at (0, kvh, page*16)
+      const int kvh = sg - (sg / p.num_kv_heads) * p.num_kv_heads;
+      tma_load_3d(st, tm_k, &sh.full_bar[slot], 0, kvh, y, policy);
+      tma_load_3d(st + kPageBytes, tm_v, &sh.full_bar[slot], 0, kvh, y, policy);
+    }
+  }
+}
+
+// One or two of a warp's pages (slots slot0 / slot1, ring phases ph0 / ph1):
+// wait for them, move them into registers, refill their slots through
+// `refill` (called once per page, before the math), then run the attention
+// math on the pages whose block ids were good. t0 / t1 are the pages' first
+// token within the sequence. A wait that runs out marks the warp's segment
+// state poisoned and the CTA aborted.
+template <int kFmt, int NT, bool kMulti, typename Refill>
+__device__ __forceinline__ void consume_pages(const PartialParams& p, CtaShared<NT>& sh,
+                                              const uint8_t* stages, int slot0, uint32_t ph0,
+                                              int slot1, uint32_t ph1, bool pair, int t0, int t1,
+                                              int ctx, WarpState<NT>& st,
+                                              const uint32_t (&qf)[NT][16],
+                                              const SegLimits<NT>& sl, float scale_log2, int g,
+                                              int c, int lane, int& poisoned, Refill&& refill) {
+  volatile int* abort = &sh.abort_flag;
+  bool ready = mbar_wait_bounded(&sh.full_bar[slot0], ph0, abort);
+  if (pair) ready = ready && mbar_wait_bounded(&sh.full_bar[slot1], ph1, abort);
+  if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
+    poisoned = 1;
+    if (lane == 0) {
+      *abort = 1;
+      griddep_wait();
+      record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
+    }
+    return;
+  }
+  const uint8_t* stg0 = stages + slot0 * kStageBytes;
+  const uint8_t* stg1 = stages + slot1 * kStageBytes;
+  const bool bad0 = sh.stage_bad[slot0] != 0, bad1 = pair && sh.stage_bad[slot1] != 0;
+  PageRegs regs[2];
+  regs[0] = load_page(stg0, stg0 + kPageBytes, g, c);
+  if (pair) regs[1] = load_page(stg1, stg1 + kPageBytes, g, c);
+  // The pages are in registers: refill their slots with the pages kStages
+  // ahead right away (warp-uniform decision), before the math.
+  if (!__any_sync(kFull, *abort != 0)) {
+    refill();
+    if (pair) refill();
+  }
+  const int nv0 = min(kBlockSize, ctx - t0), nv1 = min(kBlockSize, ctx - t1);
+  if (pair && !bad0 && !bad1) {
+    const int tk[2] = {t0, t1}, nv[2] = {nv0, nv1};
+    process_pages<kFmt, 2, NT, kMulti>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
+  } else {
+    if (bad0 || bad1) poisoned = 1;
+    if (!bad0) {
+      const PageRegs one[1] = {regs[0]};
+      const int tk[1] = {t0}, nv[1] = {nv0};
+      process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
+    }
+    if (pair && !bad1) {
+      const PageRegs one[1] = {regs[1]};
+      const int tk[1] = {t1}, nv[1] = {nv1};
+      process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
+    }
+  }
+}
+
+// Causal limits of segment s's columns for this lane (see SegLimits).
+template <int NT>
+__device__ __forceinline__ SegLimits<NT> seg_limits(const PartialParams& p, int ctx, int ncols,
+                                                    int c) {
+  SegLimits<NT> sl;
+  sl.min_lim = ctx - p.q_len;  // the first new token's last visible token
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = 8 * j + 2 * c + e;
+      sl.lim[j][e] = col < ncols ? ctx - p.q_len + col / p.group : 0x7fffffff;
+    }
+  return sl;
+}
+
+// Merge of one buffered segment by all threads (column col, dims dq..dq+3):
+// the 8 warps' (m, l, O) combine in shared memory; a segment owned whole is
+// normalised and written as fp16, a split piece goes to partial slot cta + s.
+template <int NT>
+__device__ __forceinline__ void merge_buffer(const PartialParams& p, CtaShared<NT>& sh,
+                                             const float* merge_bufs, int mb, int ncols,
+                                             float v_scale) {
+  using Geom = PartialGeom<NT>;
+  constexpr int kCols = Geom::kCols;
+  const int tid = threadIdx.x;
+  const int ms = sh.buf_seg[mb];
+  const bool mwhole = sh.buf_whole[mb] != 0;
+  int any_poison = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) any_poison |= sh.buf_poison[mb][w];
+  const float* base = merge_bufs + mb * Geom::kMergeBufFloats;
+  const float* bm = base + Geom::kScratchFloats;
+  const float* bl = bm + kWarps * kCols;
+  const int dq = (tid & 31) * 4;  // 0..124
+#pragma unroll
+  for (int col = tid >> 5; col < kCols; col += kWarps) {
+    if (col >= ncols) break;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, bm[w * kCols + col]);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = bm[w * kCols + col];
+      const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      L += sc * bl[w * kCols + col];
+      const float4 v =
+          *reinterpret_cast<const float4*>(base + (w * kCols + col) * kScratchStride + dq);
+      acc.x += sc * v.x;
+      acc.y += sc * v.y;
+      acc.z += sc * v.z;
+      acc.w += sc * v.w;
+    }
+    if (mwhole) {
+      __half* o = p.out + col_row(p, ms, col) * kHeadDim + dq;
+      if (any_poison) {
+        const float nan = __int_as_float(0x7fc00000);
+        store_half4(o, nan, nan, nan, nan);
+      } else {
+        const float rr = (L > 0.f) ? v_scale / L : 0.f;
+        store_half4(o, acc.x * rr, acc.y * rr, acc.z * rr, acc.w * rr);
+      }
+    } else {
+      float* slotp = p.partials + (size_t)(blockIdx.x + ms) * kSlotFloats;
+      *reinterpret_cast<float4*>(slotp + col * kHeadDim + dq) = acc;
+      if (dq == 0) {
+        slotp[kSlotM + col] = M;
+        slotp[kSlotL + col] = L;
+      }
+    }
+  }
+  if (!mwhole && tid == 0) {  // a split piece: its ticket is taken after the range
+    sh.pend_seg[sh.npend] = ms;
+    sh.pend_poison[sh.npend] = any_poison;
+    ++sh.npend;
+  }
+}
+
+// CTA mode: warp w takes the CTA-local pages w, w + 8, w + 16, ... of the
+// range (two at a time), keeping kLookahead of them in flight; at the end of
+// each segment every warp hands its (m, l, O) to a merge buffer, merged across
+// warps when the buffer is next reused or at the end of the range.
+template <int kFmt, int NT, bool kMulti>
+__device__ __forceinline__ void cta_mode_range(const PartialParams& p, const CUtensorMap* tm_k,
+                                               const CUtensorMap* tm_v, CtaShared<NT>& sh,
+                                               const CtaSmem<NT>& sm, const RangeView& rv,
+                                               float scale_log2, float v_scale, uint64_t policy,
+                                               WarpState<NT>& st, uint32_t (&qf)[NT][16],
+                                               uint32_t (&qf_next)[NT][16], int& q_next_seg,
+                                               int& issued, int& kseg) {
+  using Geom = PartialGeom<NT>;
+  constexpr int kCols = Geom::kCols;
+  constexpr int kBufs = Geom::kMergeBufs;
+  constexpr bool kPrefetchQ = NT == 1;  // registers: two-tile kernels load Q per segment
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
+  const int ncols = p.group * p.q_len;
+  const int32_t* segs = rv.segs;
+  const int cbeg = rv.cbeg, cend = rv.cend, npages = rv.npages;
+  const int s_first = rv.s_first, s_hi = rv.s_hi;
 
   // ---- this warp's loads: owned page k is CTA-local page warp + 8k ----
   const int owned = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
   PageBatch cur = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 0, lane);
   PageBatch nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 32, lane);
   int cur_base = 0;
-  int issued = 0;  // owned pages whose loads have been issued
   auto issue_next = [&]() {
     if (issued >= owned) return;
     const int k = issued++;
@@ -678,95 +899,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sg = __shfl_sync(kFull, cur.seg, k - cur_base);
     const int slot = (warp + kWarps * k) % kStages;
     __syncwarp();  // all lanes' reads of this slot's previous page are done
-    if (lane == 0) {
-      uint8_t* st = stages + slot * kStageBytes;
-      stage_bad[slot] = bad;
-      fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
-      if (bad) {
-        griddep_wait();  // the planner resets seg_bad and the status word
-        atomicOr(&p.seg_bad[sg], 1);
-        record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
-        mbar_arrive(&full_bar[slot]);
-      } else {
-        mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
-        if (p.kv_layout == XQA_LAYOUT_HND) {
-          tma_load_2d(st, &tm_k, &full_bar[slot], 0, y, policy);
-          tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, y, policy);
-        } else {  // NHD: box (128 dims, 1 kv head, 16 tokens) at (0, kvh, page*16)
-          const int kvh = sg - (sg / p.num_kv_heads) * p.num_kv_heads;
-          tma_load_3d(st, &tm_k, &full_bar[slot], 0, kvh, y, policy);
-          tma_load_3d(st + kPageBytes, &tm_v, &full_bar[slot], 0, kvh, y, policy);
-        }
-      }
-    }
+    if (lane == 0) issue_page<NT>(p, tm_k, tm_v, sh, sm.stages, slot, y, bad, sg, policy);
     __syncwarp();
   };
 #pragma unroll 1
   for (int i = 0; i < kLookahead; ++i) issue_next();
 
-  if (tid == 0) npend = 0;
-  WarpState<NT> st;
-  uint32_t qf[NT][16], qf_next[NT][16];
-  int q_next_seg = -1;
-  // Merge of one buffered segment by all threads (column col, dims dq..dq+3):
-  // the 8 warps' (m, l, O) combine in shared memory; a segment owned whole is
-  // normalised and written as fp16, a split piece goes to partial slot cta + s.
-  auto merge_buffer = [&](int mb) {
-    const int ms = buf_seg[mb];
-    const bool mwhole = buf_whole[mb] != 0;
-    int any_poison = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) any_poison |= buf_poison[mb][w];
-    const float* base = merge_bufs + mb * Geom::kMergeBufFloats;
-    const float* bm = base + Geom::kScratchFloats;
-    const float* bl = bm + kWarps * kCols;
-    const int dq = (tid & 31) * 4;  // 0..124
-#pragma unroll
-    for (int col = tid >> 5; col < kCols; col += kWarps) {
-      if (col >= ncols) break;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, bm[w * kCols + col]);
-      float L = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = bm[w * kCols + col];
-        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        L += sc * bl[w * kCols + col];
-        const float4 v =
-            *reinterpret_cast<const float4*>(base + (w * kCols + col) * kScratchStride + dq);
-        acc.x += sc * v.x;
-        acc.y += sc * v.y;
-        acc.z += sc * v.z;
-        acc.w += sc * v.w;
-      }
-      if (mwhole) {
-        __half* o = p.out + col_row(p, ms, col) * kHeadDim + dq;
-        if (any_poison) {
-          const float nan = __int_as_float(0x7fc00000);
-          store_half4(o, nan, nan, nan, nan);
-        } else {
-          const float rr = (L > 0.f) ? v_scale / L : 0.f;
-          store_half4(o, acc.x * rr, acc.y * rr, acc.z * rr, acc.w * rr);
-        }
-      } else {
-        float* slotp = p.partials + (size_t)(cta + ms) * kSlotFloats;
-        *reinterpret_cast<float4*>(slotp + col * kHeadDim + dq) = acc;
-        if (dq == 0) {
-          slotp[kSlotM + col] = M;
-          slotp[kSlotL + col] = L;
-        }
-      }
-    }
-    if (!mwhole && tid == 0) {  // a split piece: its ticket is taken after the range
-      pend_seg[npend] = ms;
-      pend_poison[npend] = any_poison;
-      ++npend;
-    }
-  };
-
-  int kseg = 0;  // segments of this range finished so far
   int s = s_first;
   int q0 = 0;
   while (q0 < npages) {
@@ -776,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = s / p.num_kv_heads;
     // from shared memory (the whole table, or this range's window of it): no
     // global round trip at a segment switch
-    const int ctx = ctxs[b];
+    const int ctx = rv.ctxs[b];
     const bool whole = (sb >= cbeg) && (se <= cend);
     if (kPrefetchQ && q_next_seg == s) {
 #pragma unroll
@@ -790,65 +928,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       q_next_seg = find_segment(segs, s, s_hi + 1, cbeg + qe);
       load_q<NT>(p, q_next_seg, g, c, qf_next);
     }
-    SegLimits<NT> sl;
-    sl.min_lim = ctx - p.q_len;  // the first new token's last visible token
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = 8 * j + 2 * c + e;
-        sl.lim[j][e] = col < ncols ? ctx - p.q_len + col / p.group : 0x7fffffff;
-      }
+    const SegLimits<NT> sl = seg_limits<NT>(p, ctx, ncols, c);
     reset_state<NT>(st);
     int poisoned = 0;
 
     // this warp's pages of the segment (q, and q + kWarps when pairing)
-    for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe;
-         q += (kPairs ? 2 : 1) * kWarps) {
-      const bool pair = kPairs && q + kWarps < qe;
-      const int slot0 = q % kStages, slot1 = (q + kWarps) % kStages;
-      bool ready = mbar_wait_bounded(&full_bar[slot0], (q / kStages) & 1, abort);
-      if (pair) ready = ready && mbar_wait_bounded(&full_bar[slot1], ((q + kWarps) / kStages) & 1, abort);
-      if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
-        poisoned = 1;
-        if (lane == 0) {
-          *abort = 1;
-          griddep_wait();
-          record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
-        }
-        continue;
-      }
-      const uint8_t* stg0 = stages + slot0 * kStageBytes;
-      const uint8_t* stg1 = stages + slot1 * kStageBytes;
-      const bool bad0 = stage_bad[slot0] != 0, bad1 = pair && stage_bad[slot1] != 0;
-      PageRegs regs[2];
-      regs[0] = load_page(stg0, stg0 + kPageBytes, g, c);
-      if (pair) regs[1] = load_page(stg1, stg1 + kPageBytes, g, c);
-      // The pages are in registers: refill their slots with the pages kStages
-      // ahead right away (warp-uniform decision), before the math.
-      if (!__any_sync(kFull, *abort != 0)) {
-        issue_next();
-        if (pair) issue_next();
-      }
+    for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe; q += 2 * kWarps) {
+      const bool pair = q + kWarps < qe;
       const int j0 = cbeg + q - sb;  // page index within the sequence
-      const int t0 = j0 * kBlockSize, t1 = (j0 + kWarps) * kBlockSize;
-      const int nv0 = min(kBlockSize, ctx - t0), nv1 = min(kBlockSize, ctx - t1);
-      if (kPairs && pair && !bad0 && !bad1) {
-        const int tk[2] = {t0, t1}, nv[2] = {nv0, nv1};
-        process_pages<kFmt, 2, NT, kMulti>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
-      } else {
-        if (bad0 || bad1) poisoned = 1;
-        if (!bad0) {
-          const PageRegs one[1] = {regs[0]};
-          const int tk[1] = {t0}, nv[1] = {nv0};
-          process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
-        }
-        if (pair && !bad1) {
-          const PageRegs one[1] = {regs[1]};
-          const int tk[1] = {t1}, nv[1] = {nv1};
-          process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
-        }
-      }
+      consume_pages<kFmt, NT, kMulti>(p, sh, sm.stages, q % kStages, (q / kStages) & 1,
+                                      (q + kWarps) % kStages, ((q + kWarps) / kStages) & 1, pair,
+                                      j0 * kBlockSize, (j0 + kWarps) * kBlockSize, ctx, st, qf,
+                                      sl, scale_log2, g, c, lane, poisoned, issue_next);
     }
 
     // ---- hand this segment's per-warp state to a merge buffer; a CTA-wide
@@ -857,11 +948,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int buf = kseg % kBufs;
     if (kseg >= kBufs) {
       consumer_bar();
-      merge_buffer(buf);
+      merge_buffer<NT>(p, sh, sm.merge_bufs, buf, ncols, v_scale);
       consumer_bar();
     }
     {
-      float* base = merge_bufs + buf * Geom::kMergeBufFloats;
+      float* base = sm.merge_bufs + buf * Geom::kMergeBufFloats;
       float* bm = base + Geom::kScratchFloats;
       float* bl = bm + kWarps * kCols;
 #pragma unroll
@@ -882,36 +973,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           bl[warp * kCols + 8 * j + 2 * c + 1] = st.l[j][1];
         }
       }
-      if (lane == 0) buf_poison[buf][warp] = poisoned;
+      if (lane == 0) sh.buf_poison[buf][warp] = poisoned;
       if (tid == 0) {
-        buf_seg[buf] = s;
-        buf_whole[buf] = whole ? 1 : 0;
+        sh.buf_seg[buf] = s;
+        sh.buf_whole[buf] = whole ? 1 : 0;
       }
     }
     ++kseg;
     q0 = qe;
     ++s;
   }
+}
 
-  // ---- merges still buffered (the range's last kBufs segments), in order ----
+// End of a CTA's range: the merges still buffered (the range's last kBufs
+// segments, in order), then for each split piece its bad flag and merge
+// ticket, and the merge of every segment this CTA completes. The ticket (a
+// device-wide atomic round trip) is taken once per piece after the whole
+// range, so no mid-range segment boundary stalls the CTA on it; the CTA whose
+// ticket completes a segment merges all its pieces in slot order, exactly as
+// the combine kernel would. Last, after an abort, the copies still in flight
+// are waited for.
+template <int NT>
+__device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<NT>& sh,
+                                             const CtaSmem<NT>& sm, const RangeView& rv,
+                                             float v_scale, int issued, int kseg) {
+  constexpr int kCols = PartialGeom<NT>::kCols;
+  constexpr int kBufs = PartialGeom<NT>::kMergeBufs;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int ncols = p.group * p.q_len;
   consumer_bar();
-  for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k) merge_buffer(k % kBufs);
+  for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k)
+    merge_buffer<NT>(p, sh, sm.merge_bufs, k % kBufs, ncols, v_scale);
   consumer_bar();
 
-  // ---- split pieces: flag, ticket, and merge by the CTA that finishes last ----
-  // The ticket (a device-wide atomic round trip) is taken once per piece after
-  // the whole range, so no mid-range segment boundary stalls the CTA on it.
-  // The CTA whose ticket completes a segment merges all its pieces in slot
-  // order, exactly as the combine kernel would.
+  const int npend = sh.npend;
   if (npend > 0) {
     // the cost line again, read back rather than kept live through the loop
-    const int32_t* cc = cc_base;
-    const long long line = *reinterpret_cast<volatile long long*>(&cost_line);
+    const int32_t* cc = sh.cc_base;
+    const long long line = *reinterpret_cast<volatile long long*>(&sh.cost_line);
+    const int32_t* segs = rv.segs;
+    const int n = rv.n;
     griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
     consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
     if (tid < npend) {
-      const int ps = pend_seg[tid];
-      if (pend_poison[tid]) atomicOr(&p.seg_bad[ps], 1);
+      const int ps = sh.pend_seg[tid];
+      if (sh.pend_poison[tid]) atomicOr(&p.seg_bad[ps], 1);
       int last = 0;
       if (p.fused_merge) {
         const int ilo = cta_of_vpos((long long)segs[ps] + cc[ps], line, n);
@@ -921,14 +1027,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // visible to this CTA after the next barrier
         last = (atom_add_acq_rel_gpu(&p.seg_count[ps], 1) == ihi - ilo) ? 1 : 0;
       }
-      pend_last[tid] = last;
+      sh.pend_last[tid] = last;
     }
     consumer_bar();
     int m0 = 0, m1 = 0, nm = 0;  // the segments this CTA completes (at most two)
     for (int i = 0; i < npend; ++i) {
-      if (!pend_last[i]) continue;
-      if (nm == 0) m0 = pend_seg[i];
-      else m1 = pend_seg[i];
+      if (!sh.pend_last[i]) continue;
+      if (nm == 0) m0 = sh.pend_seg[i];
+      else m1 = sh.pend_seg[i];
       ++nm;
     }
     const int ms[2] = {m0, m1};
@@ -937,9 +1043,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         merge_segments<NT == 1>(p, ms, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
   }
 
-  // Drain: after an abort some issued copies may not have been waited for; every
-  // copy must land before the CTA's shared memory is released.
-  if (*abort) {
+  // Drain: after an abort some issued copies may not have been waited for.
+  // Each is waited for once more, with the same time budget; a copy that
+  // still has not landed after that is left, and the CTA exits with the
+  // timeout already recorded.
+  if (sh.abort_flag) {
     int never = 0;
     volatile int* no_abort = &never;
     // only the last kLookahead issued pages can still be in flight: every
@@ -947,10 +1055,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int first = issued > kLookahead ? issued - kLookahead : 0;
     for (int k = first; k < issued; ++k) {
       const int q = warp + kWarps * k;
-      const bool ok = mbar_wait_bounded(&full_bar[q % kStages], (q / kStages) & 1, no_abort);
+      const bool ok = mbar_wait_bounded(&sh.full_bar[q % kStages], (q / kStages) & 1, no_abort);
       if (!__all_sync(kFull, ok)) break;
     }
   }
+  (void)ncols;
+}
+
+}  // namespace
+
+template <int kFmt, int NT, bool kMulti>
+__global__ void __launch_bounds__(kThreads, 1)
+    partial_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const PartialParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) CtaShared<NT> sh;
+  griddep_launch_dependents();  // a dependent next kernel waits for this grid itself
+  // per-tensor scales: host values, or device scalars read when the kernel runs
+  const float k_scale = p.k_scale_ptr ? __ldg(p.k_scale_ptr) : p.k_scale;
+  const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
+  const float scale_log2 = static_cast<float>(p.qk_scale_base * static_cast<double>(k_scale));
+  const CtaSmem<NT> sm = carve_smem<NT>(smem_raw);
+  RangeView rv;
+  if (!setup_range<NT>(p, &tm_k, &tm_v, sh, sm, rv)) return;
+  const uint64_t policy = l2_evict_first_policy();
+
+  WarpState<NT> st;
+  uint32_t qf[NT][16], qf_next[NT][16];
+  int q_next_seg = -1;
+  int issued = 0;  // this warp's pages whose loads have been issued
+  int kseg = 0;    // segments of this range handed to the merge buffers
+  cta_mode_range<kFmt, NT, kMulti>(p, &tm_k, &tm_v, sh, sm, rv, scale_log2, v_scale, policy, st, qf,
+                                   qf_next, q_next_seg, issued, kseg);
+  finish_range<NT>(p, sh, sm, rv, v_scale, issued, kseg);
 }
 
 // The same kernel with a second way to work a range (warp mode): when the
@@ -958,276 +1095,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 // kWarpModePages pages each, whole pieces go to single warps (round-robin over
 // the range's segments, a static rule), each warp accumulates its piece alone
 // and writes it from registers, with no merge across warps and no CTA barrier
-// per segment; other ranges are worked as above. Launched only for shapes with
-// many segments per CTA (batches of many short sequences): the extra code
-// slows the page loop of ranges worked the usual way.
+// per segment; other ranges are worked in CTA mode as above. Launched only for
+// shapes with many segments per CTA (batches of many short sequences): the
+// mode test and the warp-mode code slow the page loop of CTA-mode ranges.
 template <int kFmt, int NT, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1)
     partial_kernel_wm(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const PartialParams p) {
-  using Geom = PartialGeom<NT>;
-  constexpr int kCols = Geom::kCols;
-  constexpr int kBufs = Geom::kMergeBufs;
-  constexpr bool kPairs = true;  // two pages per warp iteration
-  constexpr bool kPrefetchQ = NT == 1;  // registers: two-tile kernels load Q per segment
+                      const PartialParams p) {
+  static_assert(NT == 1, "warp mode holds one column tile");
+  constexpr bool kPrefetchQ = true;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kStages];
-  __shared__ int stage_bad[kStages];
-  __shared__ int abort_flag;
-
-  __shared__ int scan_warp[kWarps], scan_warp_cost[kWarps];
-  __shared__ int scan_carry, scan_carry_cost;
-  __shared__ long long cost_line;  // kept here: the end of the kernel reads it back
-  __shared__ int range_lo, range_hi, range_seg, range_seg_hi;  // pages; first, last segment
-  __shared__ const int32_t* cc_base;  // the cost-line prefix the end of the kernel reads
-  // split pieces of this CTA (at most its first and last segment), whose
-  // merge tickets are taken once the whole range is done
-  __shared__ int pend_seg[2], pend_poison[2], pend_last[2];
-  __shared__ int npend;
-  // the segment each merge buffer holds, whether this CTA owns it whole, and
-  // each warp's "met a bad page" flag for it
-  __shared__ int buf_seg[kBufs], buf_whole[kBufs], buf_poison[kBufs][kWarps];
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cta = blockIdx.x;
+  __shared__ __align__(8) CtaShared<NT> sh;
   griddep_launch_dependents();  // a dependent next kernel waits for this grid itself
-  const int nseg = p.batch * p.num_kv_heads;
   const int ncols = p.group * p.q_len;
-  // per-tensor scales: host values, or device scalars read when the kernel runs
   const float k_scale = p.k_scale_ptr ? __ldg(p.k_scale_ptr) : p.k_scale;
   const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
   const float scale_log2 = static_cast<float>(p.qk_scale_base * static_cast<double>(k_scale));
-
-  uint8_t* stages = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* merge_bufs = reinterpret_cast<float*>(stages + kStages * kStageBytes);
-  int32_t* seg_cache = reinterpret_cast<int32_t*>(merge_bufs + kBufs * Geom::kMergeBufFloats);
-  int32_t* ctx_cache = seg_cache + kSegCache;  // context length per sequence
-  int32_t* cc_cache = ctx_cache + kSegCache;   // cost-line prefix per segment
-
-  // ---- the plan: computed here when the segment table fits in shared memory
-  // (same integer rule as the planner kernel), else read from the planner ----
-  const bool segs_in_smem = nseg + 1 <= kSegCache;
-  const int32_t* segs;
-  const int32_t* cc;
-  int total, n;
-  if (segs_in_smem) {
-    if (tid == 0) scan_carry = scan_carry_cost = 0;
-    __syncthreads();
-    const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
-    for (int base = 0; base < p.batch; base += kThreads) {
-      const int b = base + tid;
-      int pages = 0;
-      if (b < p.batch) {
-        const int ctx = __ldg(&p.context_lens[b]);
-        ctx_cache[b] = ctx;
-        pages = (ctx < 0 || (long long)ctx > max_ctx) ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
-      }
-      const int cost = seg_cost(pages);  // every kv head's segment of sequence b
-      int incl = pages, incl_cost = cost;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int u = __shfl_up_sync(kFull, incl, off);
-        const int uc = __shfl_up_sync(kFull, incl_cost, off);
-        if (lane >= off) {
-          incl += u;
-          incl_cost += uc;
-        }
-      }
-      if (lane == 31) {
-        scan_warp[warp] = incl;
-        scan_warp_cost[warp] = incl_cost;
-      }
-      __syncthreads();
-      int before = scan_carry, before_cost = scan_carry_cost;
-      for (int w = 0; w < warp; ++w) {
-        before += scan_warp[w];
-        before_cost += scan_warp_cost[w];
-      }
-      const int excl = before + incl - pages;
-      const int excl_cost = before_cost + incl_cost - cost;
-      if (b < p.batch)
-        for (int h = 0; h < p.num_kv_heads; ++h) {
-          seg_cache[b * p.num_kv_heads + h] = excl * p.num_kv_heads + h * pages;
-          cc_cache[b * p.num_kv_heads + h] = excl_cost * p.num_kv_heads + (h + 1) * cost;
-        }
-      __syncthreads();
-      if (tid == kThreads - 1) {
-        scan_carry = excl + pages;
-        scan_carry_cost = excl_cost + cost;
-      }
-      __syncthreads();
-    }
-    total = scan_carry * p.num_kv_heads;
-    if (tid == 0) seg_cache[nseg] = total;
-    n = num_ctas_for(total, p.n_max, p.min_pages);
-    segs = seg_cache;
-    cc = cc_cache;
-  } else {
-    griddep_wait();
-    total = p.header[2];
-    n = p.header[1];
-    segs = p.seg_start;
-    cc = p.seg_cc;
-  }
-  __syncthreads();
-
-  // ---- rows of empty segments (context length 0, or invalid -> NaN), the
-  // segments spread over every warp of every CTA (a few each) ----
-  {
-    const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
-    for (int s = cta * kWarps + warp; s < nseg; s += gridDim.x * kWarps) {
-      if (segs[s] != segs[s + 1]) continue;
-      const int ctx = __ldg(&p.context_lens[s / p.num_kv_heads]);
-      const bool bad = ctx < 0 || (long long)ctx > max_ctx;
-      const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
-      uint4 val;
-      val.x = val.y = val.z = val.w = pack_half2(v, v);
-      for (int i = lane; i < ncols * (kHeadDim / 8); i += 32) {
-        const int col = i / (kHeadDim / 8), d8 = i - col * (kHeadDim / 8);
-        reinterpret_cast<uint4*>(p.out + col_row(p, s, col) * kHeadDim)[d8] = val;
-      }
-    }
-  }
-  if (cta >= n) return;
-  // This CTA's positions [vlo, vhi) on the cost line, and the pages there: the
-  // first page at a position >= a lies in the first segment whose pages end
-  // past a. One parallel pass over the segments finds both ends (and the
-  // first segment) in shared memory, in place of two dependent searches.
-  const long long line = (long long)total + (nseg > 0 ? cc[nseg - 1] : 0);
-  const long long vlo = ((long long)cta * line) / n, vhi = ((long long)(cta + 1) * line) / n;
-  if (tid == 0) {
-    cost_line = line;
-    range_lo = range_hi = total;  // no segment ends past the position
-    range_seg = nseg;
-    range_seg_hi = nseg - 1;
-    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
-    abort_flag = 0;
-    npend = 0;
-    fence_mbar_init();
-    prefetch_tensormap(&tm_k);
-    prefetch_tensormap(&tm_v);
-  }
-  __syncthreads();
-  for (int s = tid; s < nseg; s += kThreads) {
-    const long long end = (long long)segs[s + 1] + cc[s];                 // past its last page
-    const long long prev = s > 0 ? (long long)segs[s] + cc[s - 1] : -1;  // previous one's end
-    const long long first = (long long)segs[s] + cc[s];                   // its first page
-    if (end > vlo && prev <= vlo) {
-      range_lo = vlo <= first ? segs[s] : (int)(segs[s] + (vlo - first));
-      range_seg = s;
-    }
-    if (end > vhi && prev <= vhi) {
-      range_hi = vhi <= first ? segs[s] : (int)(segs[s] + (vhi - first));
-      range_seg_hi = s;  // the range's last segment is this one or an earlier one
-    }
-  }
-  __syncthreads();
-  const int cbeg = range_lo, cend = range_hi;
-  const int npages = cend - cbeg;
-  if (npages <= 0) return;  // its share of the line is segment switch cost only
-  const int s_first = range_seg;
-  // With the planner's table in global memory, the few segments this range
-  // touches (a contiguous run) are copied into the shared caches, and the
-  // table pointers are shifted so that segment s still reads entry s.
-  int s_hi = nseg - 1;  // the last segment any lookup of this range can reach
-  const int32_t* ctxs = segs_in_smem ? ctx_cache : p.context_lens;
-  if (!segs_in_smem) {
-    const int wn = range_seg_hi - s_first + 1;
-    const int b_first = s_first / p.num_kv_heads;
-    const int wb = range_seg_hi / p.num_kv_heads - b_first + 1;
-    if (wn + 1 <= kSegCache && wb <= kSegCache) {
-      for (int i = tid; i <= wn; i += kThreads) {
-        seg_cache[i] = segs[s_first + i];
-        if (i < wn) cc_cache[i] = cc[s_first + i];
-      }
-      for (int i = tid; i < wb; i += kThreads) ctx_cache[i] = __ldg(&p.context_lens[b_first + i]);
-      __syncthreads();
-      segs = seg_cache - s_first;
-      cc = cc_cache - s_first;
-      ctxs = ctx_cache - b_first;
-      s_hi = range_seg_hi;
-    }
-  }
-  if (tid == 0) cc_base = cc;
-  volatile int* abort = &abort_flag;
+  const CtaSmem<NT> sm = carve_smem<NT>(smem_raw);
+  RangeView rv;
+  if (!setup_range<NT>(p, &tm_k, &tm_v, sh, sm, rv)) return;
   const uint64_t policy = l2_evict_first_policy();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
-
+  const int cta = blockIdx.x;
+  const int32_t* segs = rv.segs;
+  const int cbeg = rv.cbeg, cend = rv.cend;
+  const int s_first = rv.s_first;
 
   WarpState<NT> st;
   uint32_t qf[NT][16], qf_next[NT][16];
   int q_next_seg = -1;
-  // Merge of one buffered segment by all threads (column col, dims dq..dq+3):
-  // the 8 warps' (m, l, O) combine in shared memory; a segment owned whole is
-  // normalised and written as fp16, a split piece goes to partial slot cta + s.
-  auto merge_buffer = [&](int mb) {
-    const int ms = buf_seg[mb];
-    const bool mwhole = buf_whole[mb] != 0;
-    int any_poison = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) any_poison |= buf_poison[mb][w];
-    const float* base = merge_bufs + mb * Geom::kMergeBufFloats;
-    const float* bm = base + Geom::kScratchFloats;
-    const float* bl = bm + kWarps * kCols;
-    const int dq = (tid & 31) * 4;  // 0..124
-#pragma unroll
-    for (int col = tid >> 5; col < kCols; col += kWarps) {
-      if (col >= ncols) break;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, bm[w * kCols + col]);
-      float L = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = bm[w * kCols + col];
-        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        L += sc * bl[w * kCols + col];
-        const float4 v =
-            *reinterpret_cast<const float4*>(base + (w * kCols + col) * kScratchStride + dq);
-        acc.x += sc * v.x;
-        acc.y += sc * v.y;
-        acc.z += sc * v.z;
-        acc.w += sc * v.w;
-      }
-      if (mwhole) {
-        __half* o = p.out + col_row(p, ms, col) * kHeadDim + dq;
-        if (any_poison) {
-          const float nan = __int_as_float(0x7fc00000);
-          store_half4(o, nan, nan, nan, nan);
-        } else {
-          const float rr = (L > 0.f) ? v_scale / L : 0.f;
-          store_half4(o, acc.x * rr, acc.y * rr, acc.z * rr, acc.w * rr);
-        }
-      } else {
-        float* slotp = p.partials + (size_t)(cta + ms) * kSlotFloats;
-        *reinterpret_cast<float4*>(slotp + col * kHeadDim + dq) = acc;
-        if (dq == 0) {
-          slotp[kSlotM + col] = M;
-          slotp[kSlotL + col] = L;
-        }
-      }
-    }
-    if (!mwhole && tid == 0) {  // a split piece: its ticket is taken after the range
-      pend_seg[npend] = ms;
-      pend_poison[npend] = any_poison;
-      ++npend;
-    }
-  };
-
   int issued = 0;  // this warp's pages whose loads have been issued
   int kseg = 0;    // pieces handed to the merge buffers
 
-  // ---- mode: a range of at least kWarpModeMinPieces segment pieces of at
-  // most kWarpModePages pages each is worked in warp mode: whole pieces go to
-  // single warps (round-robin over the range's segments, a static rule), each
-  // accumulates its piece alone and writes it from registers, with no merge
-  // across warps and no CTA barrier per segment. Otherwise every warp takes
-  // every eighth page of the range (CTA mode). ----
-  const int nsr = find_segment(segs, s_first, s_hi + 1, cend - 1) - s_first + 1;  // segments touched
+  // ---- mode: at least kWarpModeMinPieces pieces, none longer than
+  // kWarpModePages pages -> warp mode; otherwise CTA mode ----
+  const int nsr = find_segment(segs, s_first, rv.s_hi + 1, cend - 1) - s_first + 1;  // segments touched
   bool warp_mode = false;
-  if (NT == 1 && nsr >= kWarpModeMinPieces && nsr <= kThreads) {
+  if (nsr >= kWarpModeMinPieces && nsr <= kThreads) {
     int len = 0;
     if (tid < nsr) len = min(segs[s_first + tid + 1], cend) - max(segs[s_first + tid], cbeg);
     const int pieces = __syncthreads_count(len > 0);
@@ -1236,176 +1141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (!warp_mode) {
-    // ---- this warp's loads: owned page k is CTA-local page warp + 8k ----
-    const int owned = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
-    PageBatch cur = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 0, lane);
-    PageBatch nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 32, lane);
-    int cur_base = 0;
-    auto issue_next = [&]() {
-      if (issued >= owned) return;
-      const int k = issued++;
-      if (k >= cur_base + 32) {
-        cur = nxt;
-        cur_base += 32;
-        nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, cur_base + 32, lane);
-      }
-      const int y = __shfl_sync(kFull, cur.y, k - cur_base);
-      const int bad = __shfl_sync(kFull, cur.bad, k - cur_base);
-      const int sg = __shfl_sync(kFull, cur.seg, k - cur_base);
-      const int slot = (warp + kWarps * k) % kStages;
-      __syncwarp();  // all lanes' reads of this slot's previous page are done
-      if (lane == 0) {
-        uint8_t* st = stages + slot * kStageBytes;
-        stage_bad[slot] = bad;
-        fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
-        if (bad) {
-          griddep_wait();  // the planner resets seg_bad and the status word
-          atomicOr(&p.seg_bad[sg], 1);
-          record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
-          mbar_arrive(&full_bar[slot]);
-        } else {
-          mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
-          if (p.kv_layout == XQA_LAYOUT_HND) {
-            tma_load_2d(st, &tm_k, &full_bar[slot], 0, y, policy);
-            tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, y, policy);
-          } else {  // NHD: box (128 dims, 1 kv head, 16 tokens) at (0, kvh, page*16)
-            const int kvh = sg - (sg / p.num_kv_heads) * p.num_kv_heads;
-            tma_load_3d(st, &tm_k, &full_bar[slot], 0, kvh, y, policy);
-            tma_load_3d(st + kPageBytes, &tm_v, &full_bar[slot], 0, kvh, y, policy);
-          }
-        }
-      }
-      __syncwarp();
-    };
-#pragma unroll 1
-    for (int i = 0; i < kLookahead; ++i) issue_next();
-
-    int s = s_first;
-    int q0 = 0;
-    while (q0 < npages) {
-      while (segs[s + 1] <= cbeg + q0) ++s;
-      const int sb = segs[s], se = segs[s + 1];
-      const int qe = min(se, cend) - cbeg;
-      const int b = s / p.num_kv_heads;
-      // from shared memory (the whole table, or this range's window of it): no
-      // global round trip at a segment switch
-      const int ctx = ctxs[b];
-      const bool whole = (sb >= cbeg) && (se <= cend);
-      if (kPrefetchQ && q_next_seg == s) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) qf[j][i] = qf_next[j][i];
-      } else {
-        load_q<NT>(p, s, g, c, qf);
-      }
-      if (kPrefetchQ && qe < npages) {  // prefetch Q of the next segment this CTA works on
-        q_next_seg = find_segment(segs, s, s_hi + 1, cbeg + qe);
-        load_q<NT>(p, q_next_seg, g, c, qf_next);
-      }
-      SegLimits<NT> sl;
-      sl.min_lim = ctx - p.q_len;  // the first new token's last visible token
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = 8 * j + 2 * c + e;
-          sl.lim[j][e] = col < ncols ? ctx - p.q_len + col / p.group : 0x7fffffff;
-        }
-      reset_state<NT>(st);
-      int poisoned = 0;
-
-      // this warp's pages of the segment (q, and q + kWarps when pairing)
-      for (int q = q0 + ((warp - q0 % kWarps) + kWarps) % kWarps; q < qe;
-           q += (kPairs ? 2 : 1) * kWarps) {
-        const bool pair = kPairs && q + kWarps < qe;
-        const int slot0 = q % kStages, slot1 = (q + kWarps) % kStages;
-        bool ready = mbar_wait_bounded(&full_bar[slot0], (q / kStages) & 1, abort);
-        if (pair) ready = ready && mbar_wait_bounded(&full_bar[slot1], ((q + kWarps) / kStages) & 1, abort);
-        if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
-          poisoned = 1;
-          if (lane == 0) {
-            *abort = 1;
-            griddep_wait();
-            record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
-          }
-          continue;
-        }
-        const uint8_t* stg0 = stages + slot0 * kStageBytes;
-        const uint8_t* stg1 = stages + slot1 * kStageBytes;
-        const bool bad0 = stage_bad[slot0] != 0, bad1 = pair && stage_bad[slot1] != 0;
-        PageRegs regs[2];
-        regs[0] = load_page(stg0, stg0 + kPageBytes, g, c);
-        if (pair) regs[1] = load_page(stg1, stg1 + kPageBytes, g, c);
-        // The pages are in registers: refill their slots with the pages kStages
-        // ahead right away (warp-uniform decision), before the math.
-        if (!__any_sync(kFull, *abort != 0)) {
-          issue_next();
-          if (pair) issue_next();
-        }
-        const int j0 = cbeg + q - sb;  // page index within the sequence
-        const int t0 = j0 * kBlockSize, t1 = (j0 + kWarps) * kBlockSize;
-        const int nv0 = min(kBlockSize, ctx - t0), nv1 = min(kBlockSize, ctx - t1);
-        if (kPairs && pair && !bad0 && !bad1) {
-          const int tk[2] = {t0, t1}, nv[2] = {nv0, nv1};
-          process_pages<kFmt, 2, NT, kMulti>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
-        } else {
-          if (bad0 || bad1) poisoned = 1;
-          if (!bad0) {
-            const PageRegs one[1] = {regs[0]};
-            const int tk[1] = {t0}, nv[1] = {nv0};
-            process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
-          }
-          if (pair && !bad1) {
-            const PageRegs one[1] = {regs[1]};
-            const int tk[1] = {t1}, nv[1] = {nv1};
-            process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
-          }
-        }
-      }
-
-      // ---- hand this segment's per-warp state to a merge buffer; a CTA-wide
-      // barrier only when the buffer still holds an unmerged segment (with two
-      // buffers a range of at most two segments never stops mid-way) ----
-      const int buf = kseg % kBufs;
-      if (kseg >= kBufs) {
-        consumer_bar();
-        merge_buffer(buf);
-        consumer_bar();
-      }
-      {
-        float* base = merge_bufs + buf * Geom::kMergeBufFloats;
-        float* bm = base + Geom::kScratchFloats;
-        float* bl = bm + kWarps * kCols;
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          float* my = base + (warp * kCols + 8 * j) * kScratchStride;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int d0 = 16 * g + 2 * i;
-            my[(2 * c) * kScratchStride + d0] = st.o[j][i][0];
-            my[(2 * c + 1) * kScratchStride + d0] = st.o[j][i][1];
-            my[(2 * c) * kScratchStride + d0 + 1] = st.o[j][i][2];
-            my[(2 * c + 1) * kScratchStride + d0 + 1] = st.o[j][i][3];
-          }
-          if (g == 0) {
-            bm[warp * kCols + 8 * j + 2 * c] = st.m[j][0];
-            bm[warp * kCols + 8 * j + 2 * c + 1] = st.m[j][1];
-            bl[warp * kCols + 8 * j + 2 * c] = st.l[j][0];
-            bl[warp * kCols + 8 * j + 2 * c + 1] = st.l[j][1];
-          }
-        }
-        if (lane == 0) buf_poison[buf][warp] = poisoned;
-        if (tid == 0) {
-          buf_seg[buf] = s;
-          buf_whole[buf] = whole ? 1 : 0;
-        }
-      }
-      ++kseg;
-      q0 = qe;
-      ++s;
-    }
-  } else if constexpr (NT == 1) {
+    cta_mode_range<kFmt, NT, kMulti>(p, &tm_k, &tm_v, sh, sm, rv, scale_log2, v_scale, policy, st,
+                                     qf, qf_next, q_next_seg, issued, kseg);
+  } else {
     // ---- warp mode: this warp's pieces are the range's segments j = warp,
     // warp + 8, ... (j counted from s_first; empty ones skipped). A piece's
     // block ids are fetched one per lane; the next piece's when the current
@@ -1453,30 +1191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int bad = __shfl_sync(kFull, wcur.bad, ioff);
           ++ioff;
           const int k = issued++;
-          const int sg = wcur.seg;
           const int slot = (warp + kWarps * k) % kStages;
           __syncwarp();  // all lanes' reads of this slot's previous page are done
-          if (lane == 0) {
-            uint8_t* st = stages + slot * kStageBytes;
-            stage_bad[slot] = bad;
-            fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
-            if (bad) {
-              griddep_wait();  // the planner resets seg_bad and the status word
-              atomicOr(&p.seg_bad[sg], 1);
-              record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
-              mbar_arrive(&full_bar[slot]);
-            } else {
-              mbar_arrive_expect_tx(&full_bar[slot], kStageBytes);
-              if (p.kv_layout == XQA_LAYOUT_HND) {
-                tma_load_2d(st, &tm_k, &full_bar[slot], 0, y, policy);
-                tma_load_2d(st + kPageBytes, &tm_v, &full_bar[slot], 0, y, policy);
-              } else {  // NHD: box (128 dims, 1 kv head, 16 tokens) at (0, kvh, page*16)
-                const int kvh = sg - (sg / p.num_kv_heads) * p.num_kv_heads;
-                tma_load_3d(st, &tm_k, &full_bar[slot], 0, kvh, y, policy);
-                tma_load_3d(st + kPageBytes, &tm_v, &full_bar[slot], 0, kvh, y, policy);
-              }
-            }
-          }
+          if (lane == 0) issue_page<NT>(p, &tm_k, &tm_v, sh, sm.stages, slot, y, bad, wcur.seg, policy);
           __syncwarp();
           return;
         }
@@ -1497,7 +1214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       piece(j, pb, len);
       const int sb = segs[s], se = segs[s + 1];
       const bool whole = (sb >= cbeg) && (se <= cend);
-      const int ctx = ctxs[s / p.num_kv_heads];
+      const int ctx = rv.ctxs[s / p.num_kv_heads];
       if (kPrefetchQ && q_next_seg == s) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) qf[0][i] = qf_next[0][i];
@@ -1511,58 +1228,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_q<NT>(p, q_next_seg, g, c, qf_next);
         }
       }
-      SegLimits<NT> sl;
-      sl.min_lim = ctx - p.q_len;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = 2 * c + e;
-        sl.lim[0][e] = col < ncols ? ctx - p.q_len + col / p.group : 0x7fffffff;
-      }
+      const SegLimits<NT> sl = seg_limits<NT>(p, ctx, ncols, c);
       reset_state<NT>(st);
       int poisoned = 0;
       for (int o = 0; o < len; o += 2) {
         const bool pair = o + 1 < len;
-        const int slot0 = (warp + kWarps * k) % kStages, slot1 = (warp + kWarps * (k + 1)) % kStages;
-        bool ready = mbar_wait_bounded(&full_bar[slot0], (k / kLookahead) & 1, abort);
-        if (pair) ready = ready && mbar_wait_bounded(&full_bar[slot1], ((k + 1) / kLookahead) & 1, abort);
+        const int t0 = (pb + o - sb) * kBlockSize;
+        consume_pages<kFmt, NT, kMulti>(p, sh, sm.stages, (warp + kWarps * k) % kStages,
+                                        (k / kLookahead) & 1, (warp + kWarps * (k + 1)) % kStages,
+                                        ((k + 1) / kLookahead) & 1, pair, t0, t0 + kBlockSize, ctx,
+                                        st, qf, sl, scale_log2, g, c, lane, poisoned, issue_next_w);
         k += pair ? 2 : 1;
-        if (!__all_sync(kFull, ready)) {  // warp-uniform outcome
-          poisoned = 1;
-          if (lane == 0) {
-            *abort = 1;
-            griddep_wait();
-            record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
-          }
-          continue;
-        }
-        const uint8_t* stg0 = stages + slot0 * kStageBytes;
-        const uint8_t* stg1 = stages + slot1 * kStageBytes;
-        const bool bad0 = stage_bad[slot0] != 0, bad1 = pair && stage_bad[slot1] != 0;
-        PageRegs regs[2];
-        regs[0] = load_page(stg0, stg0 + kPageBytes, g, c);
-        if (pair) regs[1] = load_page(stg1, stg1 + kPageBytes, g, c);
-        if (!__any_sync(kFull, *abort != 0)) {
-          issue_next_w();
-          if (pair) issue_next_w();
-        }
-        const int t0 = (pb + o - sb) * kBlockSize, t1 = t0 + kBlockSize;
-        const int nv0 = min(kBlockSize, ctx - t0), nv1 = min(kBlockSize, ctx - t1);
-        if (pair && !bad0 && !bad1) {
-          const int tk[2] = {t0, t1}, nv[2] = {nv0, nv1};
-          process_pages<kFmt, 2, NT, kMulti>(st, regs, qf, tk, nv, sl, scale_log2, g, c);
-        } else {
-          if (bad0 || bad1) poisoned = 1;
-          if (!bad0) {
-            const PageRegs one[1] = {regs[0]};
-            const int tk[1] = {t0}, nv[1] = {nv0};
-            process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
-          }
-          if (pair && !bad1) {
-            const PageRegs one[1] = {regs[1]};
-            const int tk[1] = {t1}, nv[1] = {nv1};
-            process_pages<kFmt, 1, NT, kMulti>(st, one, qf, tk, nv, sl, scale_log2, g, c);
-          }
-        }
       }
       // ---- the piece's (m, l, O) straight from this warp's registers: lane
       // (g, c) holds dims 16g + 2i (+1) of columns 2c, 2c + 1 ----
@@ -1596,71 +1272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!whole && lane == 0) {  // a split piece: its ticket is taken after all the work
-        const int idx = atomicAdd(&npend, 1);
-        pend_seg[idx] = s;
-        pend_poison[idx] = poisoned;
+        const int idx = atomicAdd(&sh.npend, 1);
+        sh.pend_seg[idx] = s;
+        sh.pend_poison[idx] = poisoned;
       }
     }
   }
-
-  // ---- merges still buffered (the range's last kBufs segments), in order ----
-  consumer_bar();
-  for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k) merge_buffer(k % kBufs);
-  consumer_bar();
-
-  // ---- split pieces: flag, ticket, and merge by the CTA that finishes last ----
-  // The ticket (a device-wide atomic round trip) is taken once per piece after
-  // the whole range, so no mid-range segment boundary stalls the CTA on it.
-  // The CTA whose ticket completes a segment merges all its pieces in slot
-  // order, exactly as the combine kernel would.
-  if (npend > 0) {
-    // the cost line again, read back rather than kept live through the loop
-    const int32_t* cc = cc_base;
-    const long long line = *reinterpret_cast<volatile long long*>(&cost_line);
-    griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
-    consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
-    if (tid < npend) {
-      const int ps = pend_seg[tid];
-      if (pend_poison[tid]) atomicOr(&p.seg_bad[ps], 1);
-      int last = 0;
-      if (p.fused_merge) {
-        const int ilo = cta_of_vpos((long long)segs[ps] + cc[ps], line, n);
-        const int ihi = cta_of_vpos((long long)segs[ps + 1] - 1 + cc[ps], line, n);
-        // release: this CTA's slots (ordered before by the barrier) are visible
-        // to whoever takes a later ticket; acquire: the earlier pieces are
-        // visible to this CTA after the next barrier
-        last = (atom_add_acq_rel_gpu(&p.seg_count[ps], 1) == ihi - ilo) ? 1 : 0;
-      }
-      pend_last[tid] = last;
-    }
-    consumer_bar();
-    int m0 = 0, m1 = 0, nm = 0;  // the segments this CTA completes (at most two)
-    for (int i = 0; i < npend; ++i) {
-      if (!pend_last[i]) continue;
-      if (nm == 0) m0 = pend_seg[i];
-      else m1 = pend_seg[i];
-      ++nm;
-    }
-    const int ms[2] = {m0, m1};
-    if (nm > 0)
-      for (int col = tid >> 5; col < kCols; col += kWarps)
-        merge_segments<NT == 1>(p, ms, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
-  }
-
-  // Drain: after an abort some issued copies may not have been waited for; every
-  // copy must land before the CTA's shared memory is released.
-  if (*abort) {
-    int never = 0;
-    volatile int* no_abort = &never;
-    // only the last kLookahead issued pages can still be in flight: every
-    // earlier one was waited for before its slot was reissued
-    const int first = issued > kLookahead ? issued - kLookahead : 0;
-    for (int k = first; k < issued; ++k) {
-      const int q = warp + kWarps * k;
-      const bool ok = mbar_wait_bounded(&full_bar[q % kStages], (q / kStages) & 1, no_abort);
-      if (!__all_sync(kFull, ok)) break;
-    }
-  }
+  finish_range<NT>(p, sh, sm, rv, v_scale, issued, kseg);
 }
 
 cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
