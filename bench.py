@@ -274,6 +274,38 @@ def cpu_baseline(name: str, budget_s: float = 12.0):
 # GPU arm
 # --------------------------------------------------------------------------
 
+def _device_workload(args, dev, xqa):
+    """The workload of the command line on the device: (w, q, block tables,
+    context lengths, [(K pool, V pool)] * pools, shape, workspace, out)."""
+    import numpy as np
+    import torch
+
+    from paged_fp8_kv_gqa_gb300 import workloads
+
+    if args.contexts:  # a custom length mix with the same recipe (not the headline)
+        hq, hkv = (int(x) for x in args.heads.split(","))
+        w = workloads.make_custom([int(c) for c in args.contexts.split(",")], hq, hkv, seed=7,
+                                  kv_dtype=args.kv_dtype, q_len=args.q_len)
+        args.workload = f"custom contexts {args.contexts}, {hq}/{hkv} heads"
+    else:
+        w = workloads.make_workload(args.workload, kv_dtype=args.kv_dtype, q_len=args.q_len)
+    if args.kv_layout == "nhd":
+        w = workloads.to_nhd(w)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q, bt, lens = up(w.q), up(w.block_tables), up(w.context_lens)
+    k0, v0 = up(w.k_cache), up(w.v_cache)
+    pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(args.pools - 1)]
+    shape = xqa.make_shape(q, k0, bt, min_pages_per_cta=args.min_pages,
+                           merge_mode=args.merge_mode, kv_dtype=args.kv_dtype,
+                           kv_layout=args.kv_layout)
+    ws = xqa.alloc_workspace(shape, dev)
+    out = torch.empty_like(q)
+    return w, q, bt, lens, pools, shape, ws, out
+
+
 def run_gpu(args, world, rank, local, dist):
     import numpy as np
     import torch
@@ -287,35 +319,11 @@ def run_gpu(args, world, rank, local, dist):
         xqa._lib = None  # build() above loaded the in-tree library
         xqa.LIB_PATH = os.path.abspath(args.lib)
         xqa.load_library()
-    from paged_fp8_kv_gqa_gb300 import workloads
-
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if args.contexts:  # a custom length mix with the same recipe (not the headline)
-        hq, hkv = (int(x) for x in args.heads.split(","))
-        w = workloads.make_custom([int(c) for c in args.contexts.split(",")], hq, hkv, seed=7,
-                                  kv_dtype=args.kv_dtype, q_len=args.q_len)
-        args.workload = f"custom contexts {args.contexts}, {hq}/{hkv} heads"
-    else:
-        w = workloads.make_workload(args.workload, kv_dtype=args.kv_dtype, q_len=args.q_len)
-    if args.kv_layout == "nhd":
-        w = workloads.to_nhd(w)
+    w, q, bt, lens, pools, shape, ws, out = _device_workload(args, dev, xqa)
+    k0, v0 = pools[0]
     kv_bytes = w.kv_bytes
-
-    def up(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    q, bt, lens = up(w.q), up(w.block_tables), up(w.context_lens)
-    pools = []
-    k0, v0 = up(w.k_cache), up(w.v_cache)
-    pools.append((k0, v0))
-    for _ in range(args.pools - 1):
-        pools.append((k0.clone(), v0.clone()))
-    shape = xqa.make_shape(q, k0, bt, min_pages_per_cta=args.min_pages,
-                           merge_mode=args.merge_mode, kv_dtype=args.kv_dtype,
-                           kv_layout=args.kv_layout)
-    ws = xqa.alloc_workspace(shape, dev)
-    out = torch.empty_like(q)
     stream = torch.cuda.Stream(device=dev)
     launches_per_step = xqa.xqa_kernels_per_call(shape)
 
@@ -538,6 +546,109 @@ def run_gpu(args, world, rank, local, dist):
 
 
 # --------------------------------------------------------------------------
+# phase breakdown from the diagnostic (timestamped) build
+# --------------------------------------------------------------------------
+
+STAMP_NAMES = ("entry", "inputs_readable", "range_known", "first_pages", "pages_done",
+               "merges_buffered", "tickets_taken", "exit")
+
+
+def stamp_breakdown(st, page_bytes: int):
+    """Phases of one launch from its per-CTA stamps (int [ctas, 10]: eight
+    %globaltimer values in ns, then the CTA's pages and segments). Times in
+    us, relative to the moment the launch could read its inputs (the first
+    CTA past the wait for the previous kernels)."""
+    import numpy as np
+
+    st = np.asarray(st, dtype=np.int64)
+    work = st[:, 8] > 0
+    start = st[:, 1][st[:, 1] > 0].min()
+    rel = (st[:, :8] - start) / 1e3
+    w = rel[work]
+    stream_us = w[:, 4] - w[:, 3]
+    pages = st[work, 8]
+    med = lambda a: float(np.median(a))
+    return {
+        "ctas_with_work": int(work.sum()),
+        "entry_before_inputs_us": -med(rel[:, 0]),
+        "range_known_us": med(w[:, 2]),
+        "first_pages_us": med(w[:, 3]),
+        "first_pages_last_cta_us": float(w[:, 3].max()),
+        "pages_done_median_us": med(w[:, 4]),
+        "pages_done_last_us": float(w[:, 4].max()),
+        "exit_last_us": float(rel[:, 7].max()),
+        "end_of_range_median_us": med(w[:, 7] - w[:, 4]),
+        "steady_gbs": float((pages * page_bytes / (stream_us * 1e3)).sum()),
+        "median_cta_stream_us": med(stream_us),
+        "pages_per_cta_min_max": [int(pages.min()), int(pages.max())],
+    }
+
+
+def run_stamps(args):
+    """Phase breakdown of the partial kernel from the timestamped diagnostic
+    build (never the headline: its numbers come from the library as built).
+    A CUDA graph of two decode steps is replayed; the stamps of the second
+    step, which overlaps the first as steps do in the timed run, are read
+    after each replay."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_fp8_kv_gqa_gb300 as xqa
+    from paged_fp8_kv_gqa_gb300 import build as _build
+
+    xqa._lib = None
+    xqa.LIB_PATH = _build.build(variant="stamps")
+    lib = xqa.load_library()
+    lib.xqa_diag_read_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    lib.xqa_diag_read_stamps.restype = ctypes.c_int
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    w, q, bt, lens, pools, shape, ws, out = _device_workload(args, dev, xqa)
+    stream = torch.cuda.Stream(device=dev)
+    n_ctas = shape.max_ctas or torch.cuda.get_device_properties(0).multi_processor_count
+
+    def step(i):
+        k, v = pools[i % len(pools)]
+        xqa.xqa_decode(q, k, v, bt, lens, w.k_scale, w.v_scale, out=out, workspace=ws,
+                       shape=shape, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            step(0)
+            step(1)
+    per = []
+    buf = np.zeros((n_ctas, 10), np.uint64)
+    for r in range(args.stamp_samples + 5):
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        rc = lib.xqa_diag_read_stamps(buf.ctypes.data, n_ctas, int(stream.cuda_stream))
+        if rc != 0:
+            raise RuntimeError(f"xqa_diag_read_stamps: status {rc}")
+        if r >= 5:
+            per.append(stamp_breakdown(buf.copy(), 2 * w.head_dim * w.block_size))
+    keys = [k for k in per[0] if isinstance(per[0][k], float)]
+    summary = {k: float(np.median([d[k] for d in per])) for k in keys}
+    summary["ctas_with_work"] = per[0]["ctas_with_work"]
+    summary["pages_per_cta_min_max"] = per[0]["pages_per_cta_min_max"]
+    return {"stamps": summary, "samples": len(per), "workload": args.workload,
+            "kv_bytes_per_step": w.kv_bytes,
+            "note": "medians over samples; times in us from the first CTA past the wait for "
+                    "the previous kernels; steady_gbs = sum over CTAs of pages x 4096 B over "
+                    "(pages done - first pages)"}
+
+
+# --------------------------------------------------------------------------
 # reference arm: the CPU oracle
 # --------------------------------------------------------------------------
 
@@ -662,10 +773,17 @@ def main(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lib", default="", help="path of an alternative libxqa.so build")
+    ap.add_argument("--stamps", action="store_true",
+                    help="print the partial kernel's phase breakdown from the timestamped "
+                         "diagnostic build instead of a bench line")
+    ap.add_argument("--stamp-samples", type=int, default=50)
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         raise SystemExit("--steps must be >= 1 and --warmup >= 0")
     world, rank, local = dist_env()
+    if args.stamps:
+        print(json.dumps(run_stamps(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, world, rank)
     else:

@@ -17,16 +17,21 @@
  * Conventions for every entry point:
  *   - Pointers marked "device" are CUDA device pointers (or managed memory)
  *     owned by the caller; the library never frees or retains them.
- *   - The library allocates no memory, keeps no state between calls except a
- *     per-device "kernel attributes set" flag, reads no environment variables,
- *     never calls abort/exit and never synchronises except in the
- *     xqa_read_* helpers, which say so.
+ *   - The library allocates no memory and reads no environment variables,
+ *     never calls abort/exit and never synchronises except in the xqa_read_*
+ *     helpers, which say so. Host state it keeps: a per-device "kernel
+ *     attributes set" flag and the cached cuTensorMapEncodeTiled entry point.
+ *     Device state it keeps: the XQA_STATIC_WORKSPACE_BYTES array of
+ *     xqa_decode_static_workspace (one per device, shared by every call of
+ *     that entry point). Between calls, a caller's workspace keeps the merge
+ *     tickets (all zero after every completed call) and the last call's
+ *     status words.
  *   - Work is enqueued on `stream` (a cudaStream_t; 0 = legacy default stream)
  *     on the current device. A non-OK return means nothing was enqueued unless
  *     the code is XQA_ERR_LAUNCH.
  *   - Problems only the device can see (a block id outside [0, NB), a context
  *     length outside [0, MBS*BS], a pipeline wait that ran out of time) are
- *     recorded in the status word inside the workspace (read it with
+ *     recorded in the status words inside the workspace (read them with
  *     xqa_read_status); the affected (sequence, kv head) output rows are
  *     written as NaN, and no out-of-bounds address is ever read.
  */
@@ -51,7 +56,9 @@ typedef enum xqa_status {
   /* written by the device into the workspace status word: */
   XQA_ERR_BAD_BLOCK_ID = 16,    /* block_tables entry outside [0, num_blocks) */
   XQA_ERR_CTX_TOO_LONG = 17,    /* context length < 0 or > MBS * block_size */
-  XQA_ERR_DEVICE_TIMEOUT = 18   /* a pipeline wait exceeded its time budget */
+  XQA_ERR_DEVICE_TIMEOUT = 18,  /* a pipeline wait exceeded its time budget */
+  XQA_ERR_DRAIN_TIMEOUT = 19    /* after a timeout, a copy was still in flight when its
+                                   CTA exited: the device state is not to be trusted */
 } xqa_status_t;
 
 /* KV cache code formats (xqa_shape_t.kv_dtype). */
@@ -63,7 +70,7 @@ typedef enum xqa_status {
 #define XQA_LAYOUT_NHD 1 /* [NB, BS, Hkv, D]: token-major pages */
 
 /* Problem dimensions. head_dim must be 128 and block_size 16; Hq must be a
- * multiple of Hkv with G = Hq / Hkv <= 8, and G * q_len <= 16. */
+ * multiple of Hkv, and G * q_len <= 16 with G = Hq / Hkv (so G <= 16). */
 typedef struct xqa_shape {
   int32_t batch;              /* B: sequences (one query token each), >= 1 */
   int32_t num_q_heads;        /* Hq */
@@ -73,7 +80,8 @@ typedef struct xqa_shape {
   int32_t max_blocks_per_seq; /* MBS: row length of block_tables */
   int32_t num_blocks;         /* NB: pages in the K (and V) pool */
   float sm_scale;             /* softmax scale; <= 0 selects 1/sqrt(D) */
-  int32_t max_ctas;           /* upper bound on split-KV CTAs; 0 = SM count */
+  int32_t max_ctas;           /* upper bound on split-KV CTAs; 0 = SM count;
+                                 values above 1024 are taken as 1024 */
   int32_t min_pages_per_cta;  /* planner lower bound on pages per CTA; 0 = 16 */
   int32_t merge_mode;         /* how segments split over several CTAs are merged:
                                  0 = by the last CTA to finish one (inside the
@@ -114,15 +122,26 @@ xqa_status_t xqa_kernels_per_call(const xqa_shape_t* shape, int32_t* kernels);
  *   v_scale       per-tensor V scale
  *   out           device, fp16, same shape as q, contiguous, 16-byte aligned
  *   workspace     device, >= xqa_workspace_size bytes, 256-byte aligned; holds
- *                 the plan, the split partials and the status word; contents
- *                 need no initialisation and are overwritten every call
+ *                 the plan, the split partials, the merge tickets and the
+ *                 status words. Zero-fill it once before its first use (e.g.
+ *                 cudaMemsetAsync(workspace, 0, bytes)): every call leaves the
+ *                 tickets at zero for the next. The tickets and status words
+ *                 sit at fixed offsets, so one workspace may serve calls of
+ *                 different shapes (sized for the largest). A call that is
+ *                 not run to completion (or xqa_attend_partial with
+ *                 merge_mode 1 not followed by xqa_combine) leaves it needing
+ *                 a fresh zero fill
  *
  * out[b, h, :] = sum_t softmax_t(sm_scale * <q[b,h], k_t>) * v_t over the
  * ctx_b tokens of kv head h / G, rounded to fp16 (round to nearest even).
- * Kernels enqueued: planner, split-KV partial (which also merges split
- * segments when merge_mode is 0), and with merge_mode 1 the log-sum-exp combine.
- * No host synchronisation; the call may be captured into a CUDA graph.
- * Concurrent calls must not share a workspace. */
+ * Kernels enqueued: the split-KV partial kernel, which derives the split plan
+ * itself and merges split segments when merge_mode is 0; before it the planner
+ * when the batch is too large for the partial kernel to hold the segment table
+ * (B * Hkv + 1 > 2048); with merge_mode 1 the log-sum-exp combine after it.
+ * The first kernel becomes resident while the previous kernel on the stream
+ * still runs and waits for it to complete before reading any input. No host
+ * synchronisation; the call may be captured into a CUDA graph. Concurrent
+ * calls must not share a workspace. */
 xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
                         const int32_t* block_tables, const int32_t* context_lens,
                         float k_scale, float v_scale, void* out, const xqa_shape_t* shape,
@@ -139,11 +158,13 @@ xqa_status_t xqa_decode_device_scales(const void* q, const uint8_t* k_cache,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* The three stages of xqa_decode, exposed separately so they can be timed one
- * by one. Called in this order with the same arguments they are exactly
- * xqa_decode. xqa_attend_partial is launched as a programmatic dependent of
- * the previous kernel on the stream (normally xqa_plan's) and must follow
- * xqa_plan on the same workspace. With merge_mode 0 the partial kernel merges
- * split segments itself and xqa_combine enqueues nothing. */
+ * by one. Called in this order with the same arguments they give exactly the
+ * results of xqa_decode. xqa_plan always launches the planner kernel (which
+ * publishes the plan in the workspace, see xqa_read_plan); xqa_decode
+ * launches it only when the batch needs it (see xqa_kernels_per_call), and
+ * xqa_attend_partial must then follow it on the same workspace. With
+ * merge_mode 0 the partial kernel merges split segments itself and
+ * xqa_combine enqueues nothing. */
 xqa_status_t xqa_plan(const int32_t* context_lens, const xqa_shape_t* shape, void* workspace,
                       size_t workspace_bytes, void* stream);
 xqa_status_t xqa_attend_partial(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
@@ -179,15 +200,22 @@ xqa_status_t xqa_dequant_e4m3(const uint8_t* in, size_t n, float scale, uint16_t
  * The attention kernel's budget is 1 s. Test use only. */
 xqa_status_t xqa_selftest_wait_timeout(int32_t* device_status, uint64_t budget_ns, void* stream);
 
-/* Copies the workspace status word to *device_status (an xqa_status_t value:
- * XQA_OK or one of the device-reported codes). Synchronises `stream`. */
+/* The device-reported status of the last call that used `workspace`:
+ * *device_status receives XQA_OK or the first device-reported code in CTA
+ * order (each CTA of the partial kernel writes its own status word as it
+ * exits). Copies the fixed-size header/ticket/status region (8256 bytes) to
+ * the host and synchronises `stream`. Returns XQA_ERR_WORKSPACE if the
+ * workspace holds no status (neither zero-filled nor written by a call). */
 xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void* stream);
 
 /* Copies the planner's output to host memory. Synchronises `stream`.
- *   header[4]          = {status, num_ctas, total_pages, num_segments}
+ *   header[4]          = {CTAs of the last partial launch, CTAs holding work,
+ *                         total_pages, num_segments}
  *   seg_start[B*Hkv+1] = exclusive prefix sum of pages per (sequence, kv head)
- *   seg_bad[B*Hkv]     = 1 where the segment's context length is invalid or a
- *                        bad block id was met, else 0 (may be NULL)
+ *   seg_bad[B*Hkv]     = 1 where the segment's context length is invalid,
+ *                        else 0 (may be NULL)
+ * The plan is published by the planner kernel when it runs, else by the
+ * partial kernel's first CTA.
  *   seg_cost[B*Hkv]    = inclusive prefix sum of the segments' switch costs on
  *                        the cost line the CTAs are cut on: 32 page units per
  *                        non-empty segment, 0 for an empty one (may be NULL) */
@@ -209,19 +237,22 @@ xqa_status_t xqa_read_plan(const void* workspace, const xqa_shape_t* shape, int3
  * Arguments and results are those of xqa_decode, minus the workspace: the
  * split-KV scratch comes from a fixed XQA_STATIC_WORKSPACE_BYTES array in the
  * library's device image, which every device that loads the library holds
- * until the process exits. Nothing is allocated and nothing needs clearing
- * (each call's planner rewrites every scratch word the call reads).
+ * until the process exits. Nothing is allocated. The array is zero-filled when
+ * the library's module loads on a device, and every completed call leaves it
+ * ready for the next, so nothing needs clearing.
  *
  *   - Shapes whose xqa_workspace_size exceeds XQA_STATIC_WORKSPACE_BYTES are
  *     rejected with XQA_ERR_WORKSPACE before anything is enqueued (for 152
  *     SMs: B * Hkv up to about 850 segments).
- *   - The first call on a device looks up the array's device address with
- *     cudaGetSymbolAddress (that device must be current) and caches it; make
- *     that first call before any stream capture.
+ *   - Every call looks up the array's device address with
+ *     cudaGetSymbolAddress, with the caller's device current (a host-side
+ *     lookup; nothing is cached, so a device reset that reloads the module
+ *     is followed). The first call on a device may load the library's module
+ *     there: make it before any stream capture.
  *   - All calls on a device share the one array: calls that may overlap on the
  *     GPU (different streams without ordering, or threads racing on one device)
  *     race on it and corrupt each other. Order them, e.g. on one stream.
- *   - The device status word lives in the shared array and is not exposed;
+ *   - The device status words live in the shared array and are not exposed;
  *     rows affected by a bad block id or context length still come back NaN. */
 xqa_status_t xqa_decode_static_workspace(const void* q, const uint8_t* k_cache,
                                          const uint8_t* v_cache, const int32_t* block_tables,

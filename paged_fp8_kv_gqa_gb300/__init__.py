@@ -30,6 +30,7 @@ XQA_ERR_DEVICE = 6
 XQA_ERR_BAD_BLOCK_ID = 16
 XQA_ERR_CTX_TOO_LONG = 17
 XQA_ERR_DEVICE_TIMEOUT = 18
+XQA_ERR_DRAIN_TIMEOUT = 19
 
 #: C symbols the library exports (kept in step with include/xqa.h).
 EXPORTED = (
@@ -184,8 +185,10 @@ def xqa_kernels_per_call(shape: XqaShape) -> int:
 
 
 def alloc_workspace(shape: XqaShape, device=None) -> torch.Tensor:
-    """A uint8 device buffer of xqa_workspace_size bytes (256-byte aligned by torch)."""
-    return torch.empty(xqa_workspace_size(shape), dtype=torch.uint8, device=device or "cuda")
+    """A zero-filled uint8 device buffer of xqa_workspace_size bytes (256-byte
+    aligned by torch). The library needs it zeroed once, before its first use;
+    every call leaves it ready for the next."""
+    return torch.zeros(xqa_workspace_size(shape), dtype=torch.uint8, device=device or "cuda")
 
 
 def _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, workspace, shape):
@@ -295,7 +298,7 @@ def xqa_read_plan(workspace: torch.Tensor, shape: XqaShape, stream=None) -> dict
                                         seg_start.ctypes.data, seg_bad.ctypes.data,
                                         seg_cost.ctypes.data, _stream_handle(stream)),
            "xqa_read_plan")
-    return {"status": int(header[0]), "num_ctas": int(header[1]), "total_pages": int(header[2]),
+    return {"ctas_launched": int(header[0]), "num_ctas": int(header[1]), "total_pages": int(header[2]),
             "num_segments": int(header[3]), "seg_start": seg_start, "seg_bad": seg_bad,
             "seg_cc": seg_cost}
 
@@ -303,12 +306,15 @@ def xqa_read_plan(workspace: torch.Tensor, shape: XqaShape, stream=None) -> dict
 def xqa_decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens, k_scale: float,
                                 v_scale: float, out=None, shape: XqaShape | None = None,
                                 stream=None, sm_scale: float = 0.0, max_ctas: int = 0,
-                                min_pages_per_cta: int = 0):
+                                min_pages_per_cta: int = 0, merge_mode: int = 0,
+                                kv_dtype: str = "e5m2", kv_layout: str = "hnd"):
     """xqa_decode without a workspace argument, for callers that may not allocate
     device memory: the scratch is the library's fixed per-device array (see
-    include/xqa.h). Calls that may overlap on one device must be ordered."""
+    include/xqa.h). q may be [B, Hq, D] or [B, T, Hq, D] (T new tokens per
+    sequence). Calls that may overlap on one device must be ordered."""
     if shape is None:
-        shape = make_shape(q, k_cache, block_tables, sm_scale, max_ctas, min_pages_per_cta)
+        shape = make_shape(q, k_cache, block_tables, sm_scale, max_ctas, min_pages_per_cta,
+                           merge_mode, kv_dtype=kv_dtype, kv_layout=kv_layout)
     if out is None:
         out = torch.empty_like(q)
     ptrs = (

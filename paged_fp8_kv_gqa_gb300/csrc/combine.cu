@@ -2,9 +2,11 @@
 //
 // One CTA per (sequence, kv head) segment; a thread handles one column (new
 // token x head) and 4 dims at a time. Segments processed whole by one
-// partial CTA were already written by it; this kernel writes zero rows for
-// empty segments (context length 0), NaN rows for bad segments and, for a
-// segment split over CTAs i_lo..i_hi, merges their pieces (slot i + s):
+// partial CTA, and empty segments, were already written by the partial
+// kernel. For a segment split over CTAs i_lo..i_hi this kernel reads the
+// segment's merge ticket (how many of its pieces met a bad block id), clears
+// it for the next call, and writes NaN rows if any did; otherwise it merges
+// the pieces (slot i + s):
 //   M = max_i m_i,  w_i = 2^(m_i - M),  L = sum_i w_i l_i,
 //   out = fp16(sum_i w_i o_i * (v_scale / L))    (round to nearest even).
 // This is the "merge" phase of the planner -> forward -> merge split-KV
@@ -38,20 +40,18 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams 
   const int n = p.header[1];
   const long long total = p.header[2];
   const int sb = p.seg_start[s], se = p.seg_start[s + 1];
-  const bool bad = p.seg_bad[s] != 0;
+  if (sb == se) return;  // empty: its row was written by the partial kernel
+  // the CTAs holding the first and the last page, on the plan's cost line
+  const long long line = total + p.seg_cc[p.header[3] - 1];
+  const int ilo = cta_of_vpos((long long)sb + p.seg_cc[s], line, n);
+  const int ihi = cta_of_vpos((long long)se - 1 + p.seg_cc[s], line, n);
+  if (ilo == ihi) return;  // written whole by its partial CTA
+  const bool bad = p.tickets[ilo] >= kTicketPoison;
+  __syncthreads();  // every thread has read the ticket before it is cleared
+  if (threadIdx.x == 0) p.tickets[ilo] = 0;
   const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
   for (int col = threadIdx.x >> 5; col < ncols; col += kCombineThreads / 32) {
     __half* o = p.out + combine_row(p, s, col) * kHeadDim + dq;
-    if (sb == se) {
-      const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
-      store_half4(o, v, v, v, v);
-      continue;
-    }
-    // the CTAs holding the first and the last page, on the planner's cost line
-    const long long line = total + p.seg_cc[p.header[3] - 1];
-    const int ilo = cta_of_vpos((long long)sb + p.seg_cc[s], line, n);
-    const int ihi = cta_of_vpos((long long)se - 1 + p.seg_cc[s], line, n);
-    if (ilo == ihi) continue;  // written whole by its partial CTA
     if (bad) {
       const float v = __int_as_float(0x7fc00000);
       store_half4(o, v, v, v, v);

@@ -47,6 +47,14 @@
 // the CTA whose ticket completes the segment merges all its pieces, loading
 // them (and those of its other completed segment) before using any.
 //
+// Bookkeeping across calls needs no reset kernel: a split segment's merge
+// ticket (the workspace word of the CTA holding its first page) counts the
+// pieces and the pieces that met a bad page, and the CTA that completes it
+// clears it; every CTA writes its own status word as it exits. So with the
+// segment table in shared memory a decode step is this one launch, which may
+// become resident while the previous kernel on the stream still runs and
+// waits for it before reading any input.
+//
 // Contraction-index permutation: the MMA result does not depend on how the
 // contraction index is laid out, as long as both operands use the same layout.
 // QK lane (g, c) owns dims [32c, 32c+32) of its two token rows; PV lane (g, c)
@@ -70,6 +78,34 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kNoMax = -1e30f;
 constexpr uint32_t kOnesHalf2 = 0x3C003C00u;
 constexpr unsigned kFull = 0xffffffffu;
+
+}  // namespace
+
+// Phase stamps, in diagnostic builds only (compiled with -DXQA_STAMPS; the
+// library itself is built without them): thread 0 of every CTA records
+// %globaltimer at fixed points of the kernel, kStampsPerCta per CTA, which
+// xqa_diag_read_stamps copies out. They add a few stores and skip no work.
+//   0 entry                 1 inputs readable (after the wait for the
+//   2 range known             previous kernels)
+//   3 first pages in warp 0's registers
+//   4 every warp done with its pages      5 buffered merges written
+//   6 merge tickets taken                 7 exit
+// and two counts: 8 the CTA's pages, 9 the segments its range touches.
+constexpr int kStampsPerCta = 10;
+#ifdef XQA_STAMPS
+__device__ unsigned long long g_stamps[kMaxCtas * kStampsPerCta];
+__device__ __forceinline__ void stamp(int i) {
+  if (threadIdx.x == 0) g_stamps[blockIdx.x * kStampsPerCta + i] = global_timer_ns();
+}
+__device__ __forceinline__ void stamp_count(int i, int v) {
+  if (threadIdx.x == 0) g_stamps[blockIdx.x * kStampsPerCta + i] = (unsigned long long)v;
+}
+#else
+__device__ __forceinline__ void stamp(int) {}
+__device__ __forceinline__ void stamp_count(int, int) {}
+#endif
+
+namespace {
 
 __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
@@ -336,16 +372,17 @@ __device__ __forceinline__ void store_half4(__half* o, float a, float b, float c
 // LSE merge of the split segments this CTA completed (at most two: the first
 // and the last of its range) into fp16 rows, thread: column col, dims
 // dq..dq+3. Pieces were written by other CTAs: read through L2. The bad flags
-// and, for segments of at most kFew pieces, every piece of both segments are
-// loaded before any is used (one round trip for the whole merge); in one-tile
+// (known from the merge tickets) and, for segments of at most kFew pieces,
+// every piece of both segments are loaded before any is used (one round trip
+// for the whole merge); in one-tile
 // kernels a segment of up to 16 pieces takes one round trip of its own, a
 // longer one two per 16 (two-tile kernels, short of registers: the maxima 16
 // and the sums 8 pieces per round trip).
 template <bool kWide>  // one round trip for up to 16 pieces (else 8, fewer registers)
-__device__ __forceinline__ void merge_segments(const PartialParams& p, const int (&ms)[2], int nm,
-                                               const int32_t* segs, const int32_t* cc,
-                                               long long line, int n, int col, int dq,
-                                               float v_scale) {
+__device__ __forceinline__ void merge_segments(const PartialParams& p, const int (&ms)[2],
+                                               const int (&mbad)[2], int nm, const int32_t* segs,
+                                               const int32_t* cc, long long line, int n, int col,
+                                               int dq, float v_scale) {
   if (col >= p.group * p.q_len) return;
   constexpr int kFew = 4;
   int ilo[2], ihi[2], bad[2];
@@ -357,7 +394,7 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
       const int s = ms[j];
       ilo[j] = cta_of_vpos((long long)segs[s] + cc[s], line, n);
       ihi[j] = cta_of_vpos((long long)segs[s + 1] - 1 + cc[s], line, n);
-      bad[j] = __ldcg(&p.seg_bad[s]);
+      bad[j] = mbad[j];
 #pragma unroll
       for (int k = 0; k < kFew; ++k) {
         if (ilo[j] + k <= ihi[j]) {
@@ -484,8 +521,12 @@ struct CtaShared {
   const int32_t* cc_base;  // the cost-line prefix the end of the kernel reads
   // split pieces of this CTA (at most its first and last segment), whose
   // merge tickets are taken once the whole range is done
-  int pend_seg[2], pend_poison[2], pend_last[2];
+  int pend_seg[2], pend_poison[2], pend_last[2], pend_bad[2];
   int npend;
+  int cta_status;  // first error this CTA met (XQA_OK if none), published at exit
+#ifdef XQA_STAMPS
+  int first_stamped;
+#endif
   // the segment each merge buffer holds, whether this CTA owns it whole, and
   // each warp's "met a bad page" flag for it
   int buf_seg[kBufs], buf_whole[kBufs], buf_poison[kBufs][kWarps];
@@ -531,7 +572,8 @@ struct RangeView {
 // The plan (computed here when the segment table fits in shared memory, with
 // the same integer rule as the planner kernel, else read from the planner),
 // the rows of empty segments, and this CTA's range on the cost line. Also
-// initialises the ring barriers. Returns false when this CTA holds no page.
+// initialises the ring barriers and waits for the kernels before this one on
+// the stream. Returns false when this CTA holds no page.
 template <int NT>
 __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtensorMap* tm_k,
                                             const CUtensorMap* tm_v, CtaShared<NT>& sh,
@@ -544,9 +586,27 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
   const int32_t* segs;
   const int32_t* cc;
   int total, n;
+  if (tid == 0) {  // before the wait: nothing here reads or writes global memory
+    for (int i = 0; i < kStages; ++i) mbar_init(&sh.full_bar[i], 1);
+    sh.abort_flag = 0;
+    sh.npend = 0;
+    sh.cta_status = XQA_OK;
+    sh.scan_carry = sh.scan_carry_cost = 0;
+#ifdef XQA_STAMPS
+    sh.first_stamped = 0;
+#endif
+    fence_mbar_init();
+    prefetch_tensormap(tm_k);
+    prefetch_tensormap(tm_v);
+  }
+  // Every input (and the planner's table, when it ran) is read after the
+  // kernels before this one on the stream have completed; this kernel may have
+  // become resident while they still ran (programmatic dependent launch).
+  griddep_wait();
+  stamp(1);
+  if (cta == 0 && tid == 0) p.header[0] = gridDim.x;  // status words this call writes
+  __syncthreads();
   if (segs_in_smem) {
-    if (tid == 0) sh.scan_carry = sh.scan_carry_cost = 0;
-    __syncthreads();
     const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
     for (int base = 0; base < p.batch; base += kThreads) {
       const int b = base + tid;
@@ -596,8 +656,21 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
     n = num_ctas_for(total, p.n_max, p.min_pages);
     segs = sm.seg_cache;
     cc = sm.cc_cache;
+    if (cta == 0) {  // publish the plan (read back by xqa_read_plan and the combine kernel)
+      for (int s = tid; s < nseg; s += kThreads) {
+        const int ctx = sm.ctx_cache[s / p.num_kv_heads];
+        p.seg_start[s] = sm.seg_cache[s];
+        p.seg_cc[s] = sm.cc_cache[s];
+        p.seg_bad[s] = (ctx < 0 || (long long)ctx > max_ctx) ? 1 : 0;
+      }
+      if (tid == 0) {
+        p.seg_start[nseg] = total;
+        p.header[1] = n;
+        p.header[2] = total;
+        p.header[3] = nseg;
+      }
+    }
   } else {
-    griddep_wait();
     total = p.header[2];
     n = p.header[1];
     segs = p.seg_start;
@@ -614,6 +687,7 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
       const int ctx = __ldg(&p.context_lens[s / p.num_kv_heads]);
       const bool bad = ctx < 0 || (long long)ctx > max_ctx;
       const float v = bad ? __int_as_float(0x7fc00000) : 0.0f;
+      if (bad && lane == 0) record_status(&sh.cta_status, XQA_ERR_CTX_TOO_LONG);
       uint4 val;
       val.x = val.y = val.z = val.w = pack_half2(v, v);
       for (int i = lane; i < ncols * (kHeadDim / 8); i += 32) {
@@ -634,12 +708,6 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
     sh.range_lo = sh.range_hi = total;  // no segment ends past the position
     sh.range_seg = nseg;
     sh.range_seg_hi = nseg - 1;
-    for (int i = 0; i < kStages; ++i) mbar_init(&sh.full_bar[i], 1);
-    sh.abort_flag = 0;
-    sh.npend = 0;
-    fence_mbar_init();
-    prefetch_tensormap(tm_k);
-    prefetch_tensormap(tm_v);
   }
   __syncthreads();
   for (int s = tid; s < nseg; s += kThreads) {
@@ -689,6 +757,9 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
   rv.segs = segs;
   rv.cc = cc;
   if (tid == 0) sh.cc_base = cc;
+  stamp(2);
+  stamp_count(8, rv.npages);
+  stamp_count(9, sh.range_seg_hi - rv.s_first + 1);
   return true;
 }
 
@@ -704,9 +775,7 @@ __device__ __forceinline__ void issue_page(const PartialParams& p, const CUtenso
   sh.stage_bad[slot] = bad;
   fence_proxy_async_smem();  // this slot's earlier shared reads come before the TMA writes
   if (bad) {
-    griddep_wait();  // the planner resets seg_bad and the status word
-    atomicOr(&p.seg_bad[sg], 1);
-    record_status(&p.header[0], XQA_ERR_BAD_BLOCK_ID);
+    record_status(&sh.cta_status, XQA_ERR_BAD_BLOCK_ID);
     mbar_arrive(&sh.full_bar[slot]);
   } else {
     mbar_arrive_expect_tx(&sh.full_bar[slot], kStageBytes);
@@ -742,11 +811,16 @@ __device__ __forceinline__ void consume_pages(const PartialParams& p, CtaShared<
     poisoned = 1;
     if (lane == 0) {
       *abort = 1;
-      griddep_wait();
-      record_status(&p.header[0], XQA_ERR_DEVICE_TIMEOUT);
+      record_status(&sh.cta_status, XQA_ERR_DEVICE_TIMEOUT);
     }
     return;
   }
+#ifdef XQA_STAMPS
+  if (threadIdx.x == 0 && !sh.first_stamped) {
+    sh.first_stamped = 1;
+    stamp(3);
+  }
+#endif
   const uint8_t* stg0 = stages + slot0 * kStageBytes;
   const uint8_t* stg1 = stages + slot1 * kStageBytes;
   const bool bad0 = sh.stage_bad[slot0] != 0, bad1 = pair && sh.stage_bad[slot1] != 0;
@@ -1002,9 +1076,11 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
   const int tid = threadIdx.x, warp = tid >> 5;
   const int ncols = p.group * p.q_len;
   consumer_bar();
+  stamp(4);
   for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k)
     merge_buffer<NT>(p, sh, sm.merge_bufs, k % kBufs, ncols, v_scale);
   consumer_bar();
+  stamp(5);
 
   const int npend = sh.npend;
   if (npend > 0) {
@@ -1013,40 +1089,59 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
     const long long line = *reinterpret_cast<volatile long long*>(&sh.cost_line);
     const int32_t* segs = rv.segs;
     const int n = rv.n;
-    griddep_wait();  // the planner's resets of seg_bad / seg_count are visible
     consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
     if (tid < npend) {
+      // A split segment's ticket is the word of the CTA holding its first page
+      // (unique in a call). Each piece adds 1, plus kTicketPoison if it met a
+      // bad page; the piece that brings the count to the number of pieces is
+      // the last, learns from the same atomic whether any piece was bad, and
+      // clears the word for the next call (every other piece has added to it).
       const int ps = sh.pend_seg[tid];
-      if (sh.pend_poison[tid]) atomicOr(&p.seg_bad[ps], 1);
-      int last = 0;
+      const int ilo = cta_of_vpos((long long)segs[ps] + cc[ps], line, n);
+      const int ihi = cta_of_vpos((long long)segs[ps + 1] - 1 + cc[ps], line, n);
+      const int add = 1 + (sh.pend_poison[tid] ? kTicketPoison : 0);
+      int last = 0, bad = 0;
       if (p.fused_merge) {
-        const int ilo = cta_of_vpos((long long)segs[ps] + cc[ps], line, n);
-        const int ihi = cta_of_vpos((long long)segs[ps + 1] - 1 + cc[ps], line, n);
         // release: this CTA's slots (ordered before by the barrier) are visible
         // to whoever takes a later ticket; acquire: the earlier pieces are
         // visible to this CTA after the next barrier
-        last = (atom_add_acq_rel_gpu(&p.seg_count[ps], 1) == ihi - ilo) ? 1 : 0;
+        const int old = atom_add_acq_rel_gpu(&p.tickets[ilo], add);
+        if ((old & (kTicketPoison - 1)) == ihi - ilo) {
+          last = 1;
+          bad = (old >= kTicketPoison || add > 1) ? 1 : 0;
+          p.tickets[ilo] = 0;
+        }
+      } else {
+        atomicAdd(&p.tickets[ilo], add);  // the combine kernel reads and clears it
       }
       sh.pend_last[tid] = last;
+      sh.pend_bad[tid] = bad;
     }
     consumer_bar();
-    int m0 = 0, m1 = 0, nm = 0;  // the segments this CTA completes (at most two)
+    stamp(6);
+    int m0 = 0, m1 = 0, b0 = 0, b1 = 0, nm = 0;  // the segments this CTA completes (at most two)
     for (int i = 0; i < npend; ++i) {
       if (!sh.pend_last[i]) continue;
-      if (nm == 0) m0 = sh.pend_seg[i];
-      else m1 = sh.pend_seg[i];
+      if (nm == 0) {
+        m0 = sh.pend_seg[i];
+        b0 = sh.pend_bad[i];
+      } else {
+        m1 = sh.pend_seg[i];
+        b1 = sh.pend_bad[i];
+      }
       ++nm;
     }
-    const int ms[2] = {m0, m1};
+    const int ms[2] = {m0, m1}, mbad[2] = {b0, b1};
     if (nm > 0)
       for (int col = tid >> 5; col < kCols; col += kWarps)
-        merge_segments<NT == 1>(p, ms, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
+        merge_segments<NT == 1>(p, ms, mbad, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
   }
 
   // Drain: after an abort some issued copies may not have been waited for.
-  // Each is waited for once more, with the same time budget; a copy that
-  // still has not landed after that is left, and the CTA exits with the
-  // timeout already recorded.
+  // Each is waited for once more, with the same time budget. A copy that
+  // still has not landed after that may land in this SM's shared memory after
+  // the CTA exits: the CTA then records XQA_ERR_DRAIN_TIMEOUT (in place of the
+  // timeout), which says that the device state is not to be trusted.
   if (sh.abort_flag) {
     int never = 0;
     volatile int* no_abort = &never;
@@ -1056,10 +1151,21 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
     for (int k = first; k < issued; ++k) {
       const int q = warp + kWarps * k;
       const bool ok = mbar_wait_bounded(&sh.full_bar[q % kStages], (q / kStages) & 1, no_abort);
-      if (!__all_sync(kFull, ok)) break;
+      if (!__all_sync(kFull, ok)) {
+        if ((threadIdx.x & 31) == 0) atomicExch(&sh.cta_status, XQA_ERR_DRAIN_TIMEOUT);
+        break;
+      }
     }
   }
-  (void)ncols;
+}
+
+// Every CTA of the launch writes its status word once, at exit (the words of
+// one call need no reset: the next call overwrites all it reads).
+template <int NT>
+__device__ __forceinline__ void publish_status(const PartialParams& p, CtaShared<NT>& sh) {
+  __syncthreads();
+  stamp(7);
+  if (threadIdx.x == 0) p.status[blockIdx.x] = sh.cta_status;
 }
 
 }  // namespace
@@ -1071,13 +1177,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) CtaShared<NT> sh;
   griddep_launch_dependents();  // a dependent next kernel waits for this grid itself
-  // per-tensor scales: host values, or device scalars read when the kernel runs
+  stamp(0);
+  const CtaSmem<NT> sm = carve_smem<NT>(smem_raw);
+  RangeView rv;
+  if (!setup_range<NT>(p, &tm_k, &tm_v, sh, sm, rv)) {
+    publish_status<NT>(p, sh);
+    return;
+  }
+  // per-tensor scales: host values, or device scalars read when the kernel
+  // runs (after the wait in setup_range, like every input)
   const float k_scale = p.k_scale_ptr ? __ldg(p.k_scale_ptr) : p.k_scale;
   const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
   const float scale_log2 = static_cast<float>(p.qk_scale_base * static_cast<double>(k_scale));
-  const CtaSmem<NT> sm = carve_smem<NT>(smem_raw);
-  RangeView rv;
-  if (!setup_range<NT>(p, &tm_k, &tm_v, sh, sm, rv)) return;
   const uint64_t policy = l2_evict_first_policy();
 
   WarpState<NT> st;
@@ -1088,6 +1199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cta_mode_range<kFmt, NT, kMulti>(p, &tm_k, &tm_v, sh, sm, rv, scale_log2, v_scale, policy, st, qf,
                                    qf_next, q_next_seg, issued, kseg);
   finish_range<NT>(p, sh, sm, rv, v_scale, issued, kseg);
+  publish_status<NT>(p, sh);
 }
 
 // The same kernel with a second way to work a range (warp mode): when the
@@ -1107,13 +1219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) CtaShared<NT> sh;
   griddep_launch_dependents();  // a dependent next kernel waits for this grid itself
+  stamp(0);
   const int ncols = p.group * p.q_len;
+  const CtaSmem<NT> sm = carve_smem<NT>(smem_raw);
+  RangeView rv;
+  if (!setup_range<NT>(p, &tm_k, &tm_v, sh, sm, rv)) {
+    publish_status<NT>(p, sh);
+    return;
+  }
   const float k_scale = p.k_scale_ptr ? __ldg(p.k_scale_ptr) : p.k_scale;
   const float v_scale = p.v_scale_ptr ? __ldg(p.v_scale_ptr) : p.v_scale;
   const float scale_log2 = static_cast<float>(p.qk_scale_base * static_cast<double>(k_scale));
-  const CtaSmem<NT> sm = carve_smem<NT>(smem_raw);
-  RangeView rv;
-  if (!setup_range<NT>(p, &tm_k, &tm_v, sh, sm, rv)) return;
   const uint64_t policy = l2_evict_first_policy();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -1279,13 +1395,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   finish_range<NT>(p, sh, sm, rv, v_scale, issued, kseg);
+  publish_status<NT>(p, sh);
 }
 
 cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const PartialParams& p, int n_max, cudaStream_t stream) {
-  // Programmatic dependent launch: CTAs may start while the planner (the
-  // previous kernel on the stream) still runs; the kernel waits for it with
-  // griddepcontrol.wait before reading or writing anything the planner writes.
+  // Programmatic dependent launch: CTAs may become resident while the previous
+  // kernel on the stream (the planner, or whatever the caller ran before)
+  // still runs; each waits for it with griddepcontrol.wait before reading or
+  // writing global memory.
   const int nt = (p.group * p.q_len + 7) / 8;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_max);
@@ -1336,3 +1454,20 @@ cudaError_t set_partial_attributes() {
 }
 
 }  // namespace xqa
+
+#ifdef XQA_STAMPS
+// Diagnostic builds: copies the phase stamps of the last launch (n_ctas rows
+// of kStampsPerCta %globaltimer values, ns) to host memory, then clears them.
+// Synchronises `stream`.
+extern "C" int xqa_diag_read_stamps(unsigned long long* host, int n_ctas, void* stream) {
+  if (!host || n_ctas < 1 || n_ctas > xqa::kMaxCtas) return XQA_ERR_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t bytes = (size_t)n_ctas * xqa::kStampsPerCta * sizeof(unsigned long long);
+  void* dev = nullptr;
+  if (cudaGetSymbolAddress(&dev, xqa::g_stamps) != cudaSuccess ||
+      cudaMemcpyAsync(host, dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(dev, 0, bytes, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return XQA_ERR_LAUNCH;
+  return XQA_OK;
+}
+#endif

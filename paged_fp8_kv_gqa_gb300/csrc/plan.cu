@@ -12,13 +12,14 @@
 // modes recorded on the page "[Kernel][WIP] Follow up FlashNext batch HC fusion
 // and QSA route audit" (section "Test Result"): a capacity-sized grid with
 // empty CTAs on short contexts, and fixed grids that regress long ones. The
-// plan is computed on the device so the decode step needs no host sync. It also
-// resets the status word, the bad-segment flags and the per-segment piece
-// counters of the in-kernel merge; the partial kernel, launched as its
-// programmatic dependent, waits for it before touching any of them. The
-// planner is itself launched as a programmatic dependent of the previous
-// kernel on the stream: it becomes resident early and waits for that kernel to
-// complete before it reads or writes anything.
+// plan is computed on the device so the decode step needs no host sync.
+//
+// The partial kernel derives the same plan itself whenever the segment table
+// fits in its shared memory; this kernel is launched only for larger batches
+// (and on request, through xqa_plan). It is launched as a programmatic
+// dependent of the previous kernel on the stream: it becomes resident early
+// and waits for that kernel to complete before it reads or writes anything;
+// the partial kernel, its own programmatic dependent, waits for it in turn.
 #include "xqa_device.cuh"
 #include "xqa_launch.h"
 
@@ -46,12 +47,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   int32_t* header = ws;
   int32_t* seg_start = ws + lay.seg_start_off / 4;
   int32_t* seg_bad = ws + lay.seg_bad_off / 4;
-  int32_t* seg_count = ws + lay.seg_count_off / 4;
   int32_t* seg_cc = ws + lay.seg_cc_off / 4;
   __shared__ int warp_total[kPlanWarps], warp_cost[kPlanWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) header[0] = XQA_OK;
-  __syncthreads();  // the reset comes before any thread records an error
   const long long max_ctx = (long long)max_blocks_per_seq * kBlockSize;
   auto pages_of = [&](int s, bool& bad) {
     const int ctx = context_lens[s / num_kv_heads];
@@ -93,9 +91,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   for (int s = s0; s < s1; ++s) {
     bool bad;
     const int pg = pages_of(s, bad);
-    if (bad) record_status(&header[0], XQA_ERR_CTX_TOO_LONG);
     seg_bad[s] = bad ? 1 : 0;
-    seg_count[s] = 0;
     seg_start[s] = start;
     cc += seg_cost(pg);
     seg_cc[s] = cc;  // inclusive: the switch costs of segments 0 .. s

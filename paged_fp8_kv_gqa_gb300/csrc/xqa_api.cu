@@ -41,7 +41,6 @@ xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
   if (s->batch < 1 || s->num_kv_heads < 1 || s->num_q_heads < 1) return XQA_ERR_SHAPE;
   if (s->num_q_heads % s->num_kv_heads != 0) return XQA_ERR_SHAPE;
   const int group = s->num_q_heads / s->num_kv_heads;
-  if (group > xqa::kMaxGroup) return XQA_ERR_SHAPE;
   if (s->max_blocks_per_seq < 1 || s->num_blocks < 1) return XQA_ERR_SHAPE;
   if (s->max_ctas < 0 || s->min_pages_per_cta < 0) return XQA_ERR_SHAPE;
   if (s->merge_mode != 0 && s->merge_mode != 1) return XQA_ERR_SHAPE;
@@ -77,7 +76,7 @@ xqa_status_t resolve(const xqa_shape_t* s, Resolved* r) {
       return XQA_ERR_DEVICE;
     r->n_max = sms;
   }
-  if (r->n_max > 65535) r->n_max = 65535;
+  if (r->n_max > xqa::kMaxCtas) r->n_max = xqa::kMaxCtas;
   r->ws = xqa::ws_layout(r->nseg, r->n_max);
   return XQA_OK;
 }
@@ -142,6 +141,10 @@ xqa_status_t encode_pool_map(CUtensorMap* map, const uint8_t* pool, const Resolv
 
 int32_t* ws_i32(void* ws) { return reinterpret_cast<int32_t*>(ws); }
 
+// The partial kernel derives the plan itself when its segment table fits in
+// shared memory; larger batches need the planner kernel first.
+bool needs_planner(const Resolved& r) { return r.nseg + 1 > xqa::kSegCache; }
+
 }  // namespace
 
 extern "C" {
@@ -160,7 +163,7 @@ xqa_status_t xqa_kernels_per_call(const xqa_shape_t* shape, int32_t* kernels) {
   Resolved r;
   xqa_status_t st = resolve(shape, &r);
   if (st != XQA_OK) return st;
-  *kernels = 2 + (r.merge_mode == 1 ? 1 : 0);  // planner, partial (+ combine)
+  *kernels = (needs_planner(r) ? 1 : 0) + 1 + (r.merge_mode == 1 ? 1 : 0);
   return XQA_OK;
 }
 
@@ -203,10 +206,11 @@ xqa_status_t attend_partial_impl(const void* q, const uint8_t* k_cache, const ui
   p.context_lens = context_lens;
   p.out = reinterpret_cast<__half*>(out);
   p.header = ws_i32(workspace);
-  p.seg_start = reinterpret_cast<const int32_t*>(base + r.ws.seg_start_off);
+  p.seg_start = reinterpret_cast<int32_t*>(base + r.ws.seg_start_off);
   p.seg_bad = reinterpret_cast<int32_t*>(base + r.ws.seg_bad_off);
-  p.seg_count = reinterpret_cast<int32_t*>(base + r.ws.seg_count_off);
-  p.seg_cc = reinterpret_cast<const int32_t*>(base + r.ws.seg_cc_off);
+  p.seg_cc = reinterpret_cast<int32_t*>(base + r.ws.seg_cc_off);
+  p.tickets = reinterpret_cast<int32_t*>(base + r.ws.ticket_off);
+  p.status = reinterpret_cast<int32_t*>(base + r.ws.status_off);
   p.partials = reinterpret_cast<float*>(base + r.ws.partials_off);
   p.n_max = r.n_max;
   p.min_pages = r.min_pages;
@@ -244,8 +248,8 @@ xqa_status_t combine_impl(const int32_t* context_lens, float v_scale, const floa
   p.out = reinterpret_cast<__half*>(out);
   p.header = ws_i32(workspace);
   p.seg_start = reinterpret_cast<const int32_t*>(base + r.ws.seg_start_off);
-  p.seg_bad = reinterpret_cast<const int32_t*>(base + r.ws.seg_bad_off);
   p.seg_cc = reinterpret_cast<const int32_t*>(base + r.ws.seg_cc_off);
+  p.tickets = reinterpret_cast<int32_t*>(base + r.ws.ticket_off);
   p.partials = reinterpret_cast<const float*>(base + r.ws.partials_off);
   p.num_q_heads = r.hq;
   p.num_kv_heads = r.hkv;
@@ -289,7 +293,8 @@ xqa_status_t xqa_decode(const void* q, const uint8_t* k_cache, const uint8_t* v_
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return XQA_ERR_ALIGN;
   if ((st = ensure_device_setup()) != XQA_OK) return st;
-  if ((st = xqa_plan(context_lens, shape, workspace, workspace_bytes, stream)) != XQA_OK)
+  if (needs_planner(r) &&
+      (st = xqa_plan(context_lens, shape, workspace, workspace_bytes, stream)) != XQA_OK)
     return st;
   if ((st = xqa_attend_partial(q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale,
                                out, shape, workspace, workspace_bytes, stream)) != XQA_OK)
@@ -312,7 +317,8 @@ xqa_status_t xqa_decode_device_scales(const void* q, const uint8_t* k_cache,
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return XQA_ERR_ALIGN;
   if ((st = ensure_device_setup()) != XQA_OK) return st;
-  if ((st = xqa_plan(context_lens, shape, workspace, workspace_bytes, stream)) != XQA_OK)
+  if (needs_planner(r) &&
+      (st = xqa_plan(context_lens, shape, workspace, workspace_bytes, stream)) != XQA_OK)
     return st;
   if ((st = attend_partial_impl(q, k_cache, v_cache, block_tables, context_lens, 0.f, 0.f,
                                 k_scale, v_scale, out, shape, workspace, workspace_bytes,
@@ -350,10 +356,23 @@ xqa_status_t xqa_selftest_wait_timeout(int32_t* device_status, uint64_t budget_n
 xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void* stream) {
   if (!workspace || !device_status) return XQA_ERR_NULL;
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(device_status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+  // header, tickets and status words: one copy of a fixed-size region
+  const xqa::WsLayout lay = xqa::ws_layout(0, 0);
+  static_assert(xqa::kMaxCtas <= 1024, "status region copied through the stack");
+  int32_t words[xqa::kHeaderWords + 2 * xqa::kMaxCtas];
+  if (cudaMemcpyAsync(words, workspace, lay.seg_start_off, cudaMemcpyDeviceToHost, s) !=
           cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return XQA_ERR_LAUNCH;
+  const int32_t launched = words[0];
+  const int32_t* status = words + lay.status_off / 4;
+  *device_status = XQA_OK;
+  if (launched < 0 || launched > xqa::kMaxCtas) return XQA_ERR_WORKSPACE;  // never written
+  for (int i = 0; i < launched; ++i)
+    if (status[i] != XQA_OK) {
+      *device_status = status[i];
+      break;
+    }
   return XQA_OK;
 }
 
@@ -393,6 +412,8 @@ const char* xqa_status_string(xqa_status_t status) {
     case XQA_ERR_BAD_BLOCK_ID: return "device: block table entry outside [0, num_blocks)";
     case XQA_ERR_CTX_TOO_LONG: return "device: context length < 0 or > max_blocks_per_seq*16";
     case XQA_ERR_DEVICE_TIMEOUT: return "device: pipeline wait exceeded its time budget";
+    case XQA_ERR_DRAIN_TIMEOUT:
+      return "device: a copy was still in flight when its CTA gave up; device state not trusted";
   }
   return "unknown status";
 }

@@ -16,8 +16,9 @@ namespace xqa {
 // ---------------------------------------------------------------------------
 constexpr int kHeadDim = 128;
 constexpr int kBlockSize = 16;
-constexpr int kMaxGroup = 8;                                  // q heads per kv head (MMA N = 8)
-constexpr int kMaxCols = 16;  // columns (new token x head) per kv head: G * q_len <= 16
+// Columns (new token x q head) per kv head: G * q_len <= 16, in one or two
+// 8-wide MMA tiles (so G <= 16: G = 16 takes both tiles for one new token).
+constexpr int kMaxCols = 16;
 constexpr int kPageBytes = kBlockSize * kHeadDim;             // one (page, kv head) slice: 2048 B
 constexpr int kStageBytes = 2 * kPageBytes;                   // K slice + V slice
 constexpr int kWarps = 8;                                     // every warp loads and computes
@@ -58,7 +59,7 @@ constexpr int kWarpModePages = 32;
 // planner's SM starts when the planner exits; the planner therefore does one
 // scan and a single round of loads whatever the batch.
 constexpr int kPlanThreads = 256;
-constexpr int kCombineThreads = kMaxGroup * 32;               // (head, 4 dims) per thread
+constexpr int kCombineThreads = 256;  // 8 warps: a warp per column, 4 dims per lane
 
 // Partial-result slot: O[col][128] unnormalised fp32, then M[col] (log2 domain),
 // L[col], for up to kMaxCols columns.
@@ -72,11 +73,22 @@ constexpr unsigned long long kWaitBudgetNs = 1000000000ull;  // 1 s
 // ---------------------------------------------------------------------------
 // workspace layout (int32 words, then 256-byte aligned fp32 partials)
 // ---------------------------------------------------------------------------
+// Upper bound on the CTAs of one partial launch (max_ctas is clamped to it).
+// The merge-ticket and status regions below are sized by it, not by the
+// shape, so they sit at the same offsets whatever shape uses the workspace.
+constexpr int kMaxCtas = 1024;
+// A split segment's merge ticket counts its finished pieces in the low 16 bits
+// and its pieces that met a bad page in the high 16 bits.
+constexpr int kTicketPoison = 1 << 16;
+constexpr int kHeaderWords = 16;
+
 struct WsLayout {
-  // header[0] status, [1] num_ctas, [2] total_pages, [3] num_segments
+  // header[0] CTAs of the last partial launch (status words written),
+  // [1] CTAs holding work, [2] total pages, [3] segments
+  size_t ticket_off;     // int32 [kMaxCtas]: merge tickets, zero between calls
+  size_t status_off;     // int32 [kMaxCtas]: each CTA's status in the last call
   size_t seg_start_off;  // int32 [nseg + 1]
-  size_t seg_bad_off;    // int32 [nseg]
-  size_t seg_count_off;  // int32 [nseg]: pieces finished, for the in-kernel merge
+  size_t seg_bad_off;    // int32 [nseg]: 1 where the context length is invalid
   size_t seg_cc_off;     // int32 [nseg]: cost of segments 0..s (inclusive), see seg_cost
   size_t partials_off;   // float [(n_max + nseg) * kSlotFloats]
   size_t total;
@@ -84,10 +96,11 @@ struct WsLayout {
 
 __host__ __device__ inline WsLayout ws_layout(long long nseg, long long n_max) {
   WsLayout l;
-  l.seg_start_off = 16;
+  l.ticket_off = 4 * kHeaderWords;
+  l.status_off = l.ticket_off + 4 * (size_t)kMaxCtas;
+  l.seg_start_off = l.status_off + 4 * (size_t)kMaxCtas;
   l.seg_bad_off = l.seg_start_off + 4 * (size_t)(nseg + 1);
-  l.seg_count_off = l.seg_bad_off + 4 * (size_t)nseg;
-  l.seg_cc_off = l.seg_count_off + 4 * (size_t)nseg;
+  l.seg_cc_off = l.seg_bad_off + 4 * (size_t)nseg;
   size_t end = l.seg_cc_off + 4 * (size_t)nseg;
   l.partials_off = (end + 255) & ~(size_t)255;
   l.total = l.partials_off + (size_t)(n_max + nseg) * kSlotFloats * sizeof(float);
@@ -334,7 +347,8 @@ struct KvConv<XQA_KV_E4M3> {
   }
 };
 
-__device__ __forceinline__ void record_status(int32_t* status, int code) {
+// First error of a CTA wins (status lives in shared memory until the CTA exits).
+__device__ __forceinline__ void record_status(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 

@@ -12,12 +12,13 @@ struct PartialParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   __half* out;
-  int32_t* header;           // workspace header (status, num_ctas, total_pages, nseg)
-  const int32_t* seg_start;  // [nseg + 1]
-  int32_t* seg_bad;          // [nseg]
-  int32_t* seg_count;        // [nseg] pieces finished (in-kernel merge tickets)
-  const int32_t* seg_cc;     // [nseg] cost-line prefix (planner's; see seg_cost)
-  float* partials;           // [(n_max + nseg) * kSlotFloats]
+  int32_t* header;     // workspace header (CTAs launched, CTAs with work, pages, segments)
+  int32_t* seg_start;  // [nseg + 1]; written here when the plan is derived in the kernel
+  int32_t* seg_bad;    // [nseg] bad context-length flags (plan output)
+  int32_t* seg_cc;     // [nseg] cost-line prefix (see seg_cost)
+  int32_t* tickets;    // [kMaxCtas] merge tickets of split segments, zero between calls
+  int32_t* status;     // [kMaxCtas] each CTA's status in this call
+  float* partials;     // [(n_max + nseg) * kSlotFloats]
   int batch, num_q_heads, num_kv_heads, group, max_blocks_per_seq, num_blocks;
   int q_len;                 // new tokens per sequence (q, out: [B, q_len, Hq, D])
   int n_max, min_pages;      // split rule inputs (same values the planner got)
@@ -33,8 +34,8 @@ struct CombineParams {
   __half* out;
   const int32_t* header;
   const int32_t* seg_start;
-  const int32_t* seg_bad;
   const int32_t* seg_cc;
+  int32_t* tickets;  // read for the bad-piece count, then cleared
   const float* partials;
   int num_q_heads, num_kv_heads, group, q_len;
   float v_scale;

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, 1, 2, 3, 4, 5, 6, 16, 17, 18):
+    for code in (0, 1, 2, 3, 4, 5, 6, 16, 17, 18, 19):
         s = xqa.xqa_status_string(code)
         assert s and s != "unknown status"
     assert xqa.xqa_status_string(12345) == "unknown status"
@@ -52,15 +52,16 @@ def test_host_validation_without_device(lib):
     n = ctypes.c_size_t(0)
     assert lib.xqa_workspace_size(ctypes.byref(shape), ctypes.byref(n)) == xqa.XQA_OK
     nseg = 64
-    # header, segment starts, bad flags, piece counters, cost-line prefix
-    head = 16 + 4 * (nseg + 1) + 4 * nseg + 4 * nseg + 4 * nseg
+    # header, merge tickets and status words (fixed size: 1024 CTAs at most),
+    # then segment starts, bad-context flags and the cost-line prefix
+    head = 64 + 4 * 1024 + 4 * 1024 + 4 * (nseg + 1) + 4 * nseg + 4 * nseg
     head = (head + 255) // 256 * 256
     assert n.value == head + (152 + nseg) * (16 * 128 + 32) * 4
     for bad in (
         xqa.XqaShape(16, 32, 4, 64, 16, 1200, 22240, 0.0, 152, 0),   # head_dim
         xqa.XqaShape(16, 32, 4, 128, 32, 1200, 22240, 0.0, 152, 0),  # block size
         xqa.XqaShape(16, 30, 4, 128, 16, 1200, 22240, 0.0, 152, 0),  # Hq % Hkv
-        xqa.XqaShape(16, 64, 4, 128, 16, 1200, 22240, 0.0, 152, 0),  # G = 16
+        xqa.XqaShape(16, 128, 4, 128, 16, 1200, 22240, 0.0, 152, 0),  # G = 32
         xqa.XqaShape(0, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0),   # batch
         xqa.XqaShape(16, 32, 4, 128, 16, 1200, 2**28, 0.0, 152, 0),  # pool too large for int32 rows
         xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0, 2),  # merge mode
@@ -69,6 +70,10 @@ def test_host_validation_without_device(lib):
         xqa.XqaShape(16, 32, 4, 128, 16, 1200, 22240, 0.0, 152, 0, 0, 0, 0, 3),  # G * T > 16
     ):
         assert lib.xqa_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == xqa.XQA_ERR_SHAPE
+    g16 = xqa.XqaShape(16, 64, 4, 128, 16, 1200, 22240, 0.0, 152, 0)  # G = 16, one token
+    assert lib.xqa_workspace_size(ctypes.byref(g16), ctypes.byref(n)) == xqa.XQA_OK
+    g16t2 = xqa.XqaShape(16, 64, 4, 128, 16, 1200, 22240, 0.0, 152, 0, 0, 0, 0, 2)
+    assert lib.xqa_workspace_size(ctypes.byref(g16t2), ctypes.byref(n)) == xqa.XQA_ERR_SHAPE
     assert lib.xqa_workspace_size(None, ctypes.byref(n)) == xqa.XQA_ERR_NULL
     assert lib.xqa_decode(None, None, None, None, None, 1.0, 1.0, None, ctypes.byref(shape), None,
                           0, None) == xqa.XQA_ERR_NULL
@@ -121,3 +126,26 @@ def test_argument_checks_come_before_any_device_call(lib):
     assert xqa.xqa_workspace_size(big) > static_bytes
     assert lib.xqa_decode_static_workspace(q, k, v, bt, lens, 1.0, 1.0, out, ctypes.byref(big),
                                            None) == xqa.XQA_ERR_WORKSPACE
+
+
+def test_kernels_per_call(lib):
+    # the partial kernel derives the plan itself while the segment table fits
+    # in shared memory (B*Hkv + 1 <= 2048 entries); larger batches add the
+    # planner kernel, merge_mode 1 the combine kernel
+    def count(batch, merge_mode=0):
+        sh = xqa.XqaShape(batch, 32, 4, 128, 16, 64, 4096, 0.0, 152, 0, merge_mode)
+        k = ctypes.c_int32(0)
+        assert lib.xqa_kernels_per_call(ctypes.byref(sh), ctypes.byref(k)) == xqa.XQA_OK
+        return k.value
+    assert count(16) == 1
+    assert count(511) == 1          # 2044 segments + 1 entries fit
+    assert count(512) == 2          # 2048 segments + 1 do not
+    assert count(16, merge_mode=1) == 2
+    assert count(512, merge_mode=1) == 3
+    assert lib.xqa_kernels_per_call(None, ctypes.byref(ctypes.c_int32())) == xqa.XQA_ERR_NULL
+
+
+def test_max_ctas_is_clamped_to_the_ticket_region():
+    a = xqa.xqa_workspace_size(xqa.XqaShape(16, 32, 4, 128, 16, 64, 4096, 0.0, 1024, 0))
+    b = xqa.xqa_workspace_size(xqa.XqaShape(16, 32, 4, 128, 16, 64, 4096, 0.0, 5000, 0))
+    assert a == b

@@ -59,3 +59,20 @@ def test_quantile_matches_numpy_linear():
         v = sorted(rng.normal(size=n).tolist())
         for q in (0.0, 0.1, 0.5, 0.9, 1.0):
             assert abs(bench._quantile(v, q) - np.quantile(v, q)) < 1e-12
+
+
+def test_stamp_breakdown_on_synthetic_stamps():
+    # three CTAs past the wait at t = 1000 ns; CTA 2 holds no pages
+    st = np.zeros((3, 10), np.int64)
+    st[0, :8] = [500, 1000, 1500, 3000, 43000, 44000, 45000, 46000]
+    st[1, :8] = [600, 1100, 1600, 3500, 45000, 45500, 47000, 48000]
+    st[2, :8] = [700, 1200, 0, 0, 0, 0, 0, 1300]
+    st[0, 8:] = [100, 1]
+    st[1, 8:] = [120, 2]
+    b = bench.stamp_breakdown(st, 4096)
+    assert b["ctas_with_work"] == 2
+    assert b["first_pages_us"] == 2.25 and b["first_pages_last_cta_us"] == 2.5
+    assert b["pages_done_last_us"] == 44.0 and b["exit_last_us"] == 47.0
+    rate = 100 * 4096 / 40000 + 120 * 4096 / 41500  # bytes per ns = GB/s
+    assert abs(b["steady_gbs"] - rate) < 1e-9
+    assert b["pages_per_cta_min_max"] == [100, 120]

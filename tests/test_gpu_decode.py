@@ -135,7 +135,7 @@ def test_one_long_sequence_split_over_every_cta(q_len):
     assert_close(a, ref, f"one 128K sequence, {q_len} new tokens")
 
 
-def test_single_token_context_is_the_v_row_bitwise():
+def test_single_token_context_is_the_v_row_by_value():
     w = wl.make_custom([1, 1, 1], 16, 2, seed=21, k_scale=0.5, v_scale=0.25)
     out = run(w)
     for b in range(3):
@@ -147,8 +147,9 @@ def test_single_token_context_is_the_v_row_bitwise():
             assert np.array_equal(out[b, h].astype(np.float64), want.astype(np.float64))
 
 
-@pytest.mark.parametrize("hq,hkv", [(4, 4), (16, 4), (8, 1), (24, 3), (2, 2)])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (16, 4), (8, 1), (24, 3), (2, 2), (32, 2), (16, 1)])
 def test_group_sizes(hq, hkv):
+    # G up to 8 fills one 8-column MMA tile; G = 16 takes two
     w = wl.make_custom([1, 16, 17, 300, 2049], hq, hkv, seed=hq * 100 + hkv)
     assert_close(run(w), oracle_of(w), f"G={hq // hkv}")
 
@@ -173,26 +174,87 @@ def test_custom_sm_scale():
     assert_close(run(w, sm_scale=0.02), oracle_of(w, sm_scale=0.02), "sm_scale")
 
 
-def test_plan_matches_oracle_bit_exactly():
+@pytest.mark.parametrize("planner", [False, True])
+def test_plan_matches_oracle_bit_exactly(planner):
+    # planner=False: the plan the partial kernel derives itself (its CTA 0
+    # publishes it); planner=True: the planner kernel, launched on request
     for ctxs, hkv, mbs_extra, max_ctas, minp in [
         ([256], 1, 0, 0, 0),
         (list(wl.BOUNDARY_CONTEXTS), 4, 0, 0, 0),
         ([5, 0, 17, 1000, 3], 2, 3, 5, 2),
         (list(range(0, 3000, 97)), 3, 0, 152, 1),
+        ([None, 70, None, 16], 2, 0, 0, 0),  # None: an invalid context length
     ]:
-        w = wl.make_custom(ctxs, hkv * 2, hkv, seed=1)
+        w = wl.make_custom([1 if c is None else c for c in ctxs], hkv * 2, hkv, seed=1)
+        for i, c in enumerate(ctxs):
+            if c is None:  # negative, then longer than the table row
+                w.context_lens[i] = -4 if i == 0 else w.max_blocks_per_seq * 16 + 1
         d = Dev(w, max_ctas=max_ctas, min_pages=minp)
-        d.run()
+        if planner:
+            xqa.xqa_plan(d.lens, d.ws, d.shape)
+        else:
+            d.run()
         got = xqa.xqa_read_plan(d.ws, d.shape)
         n_max = max_ctas or torch.cuda.get_device_properties(0).multi_processor_count
         ref = plan.plan(w.context_lens, hkv, w.max_blocks_per_seq, n_max, minp or 16)
-        assert got["status"] == 0
+        if not planner:
+            assert got["ctas_launched"] == n_max
         assert np.array_equal(got["seg_start"], ref["seg_start"])
         assert np.array_equal(got["seg_cc"], ref["seg_cc"])
         assert np.array_equal(got["seg_bad"].astype(bool), ref["seg_bad"])
         assert got["num_ctas"] == ref["num_ctas"]
         assert got["total_pages"] == ref["total_pages"]
         assert got["num_segments"] == ref["num_segments"]
+
+
+def _tickets(d: Dev) -> np.ndarray:
+    """The workspace's merge-ticket words (bytes 64 .. 64 + 4*1024)."""
+    torch.cuda.synchronize()
+    return d.ws[64:64 + 4 * 1024].cpu().numpy().view(np.int32)
+
+
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_merge_tickets_are_zero_after_every_call(merge_mode):
+    # the workspace is zeroed once; every call (good, with a bad block id, or a
+    # bad context length) must leave the tickets at zero for the next one
+    w = wl.make_custom([40, 300, 5000, 17, 2049], 8, 2, seed=71)
+    d = Dev(w, max_ctas=9, merge_mode=merge_mode)  # most segments split
+    ref = oracle_of(w)
+    d.run()
+    assert np.all(_tickets(d) == 0)
+    assert_close(d.result(), ref, "first call")
+    d.bt[2, 7] = w.num_blocks + 1  # a split segment meets a bad page
+    d.run()
+    assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
+    assert np.all(_tickets(d) == 0)
+    assert np.all(np.isnan(d.result()[2].astype(np.float32)))
+    d.bt.copy_(to_dev(w.block_tables))
+    d.lens[1] = w.max_blocks_per_seq * 16 + 5
+    d.run()
+    assert d.status() == xqa.XQA_ERR_CTX_TOO_LONG
+    assert np.all(_tickets(d) == 0)
+    d.lens.copy_(to_dev(w.context_lens))
+    d.run()
+    assert d.status() == xqa.XQA_OK
+    assert_close(d.result(), ref, "after the bad calls")
+
+
+def test_one_workspace_serves_several_shapes():
+    # the ticket and status regions sit at fixed offsets, so a workspace sized
+    # for the largest shape can be used by calls of different shapes in turn
+    ws_list = [wl.make_custom([3000, 20, 700], 32, 4, seed=72),
+               wl.make_custom([1, 16, 17, 4097, 9000, 33, 64, 2], 16, 2, seed=73),
+               wl.make_custom([5000], 8, 8, seed=74)]
+    devs = [Dev(w, max_ctas=m) for w, m in zip(ws_list, (0, 37, 5))]
+    shared = torch.zeros(max(d.ws.numel() for d in devs), dtype=torch.uint8, device="cuda")
+    for rnd in range(2):
+        for d in devs:
+            d.ws = shared[:d.ws.numel()]
+            d.out.fill_(float("nan"))
+            d.run()
+            assert d.status() == xqa.XQA_OK
+            assert_close(d.result(), oracle_of(d.w), f"round {rnd}")
+            assert np.all(_tickets(d) == 0)
 
 
 def test_cuda_graph_replay_with_changed_inputs():
@@ -285,9 +347,9 @@ def test_host_side_errors():
     rc = lib.xqa_decode(None, d.k.data_ptr(), d.v.data_ptr(), d.bt.data_ptr(), d.lens.data_ptr(),
                         1.0, 1.0, d.out.data_ptr(), d.shape, d.ws.data_ptr(), d.ws.numel(), None)
     assert rc == xqa.XQA_ERR_NULL
-    gqa16 = xqa.XqaShape(1, 16, 1, 128, 16, 16, 16, 0.0, 0, 0)
+    gqa32 = xqa.XqaShape(1, 32, 1, 128, 16, 16, 16, 0.0, 0, 0)
     with pytest.raises(xqa.XqaError) as e:
-        xqa.xqa_workspace_size(gqa16)
+        xqa.xqa_workspace_size(gqa32)
     assert e.value.code == xqa.XQA_ERR_SHAPE
 
 
