@@ -626,7 +626,7 @@ def run_stamps(args):
         with torch.cuda.graph(g, stream=stream):
             step(0)
             step(1)
-    per = []
+    per, raw = [], []
     buf = np.zeros((n_ctas, 10), np.uint64)
     for r in range(args.stamp_samples + 5):
         with torch.cuda.stream(stream):
@@ -637,15 +637,24 @@ def run_stamps(args):
             raise RuntimeError(f"xqa_diag_read_stamps: status {rc}")
         if r >= 5:
             per.append(stamp_breakdown(buf.copy(), 2 * w.head_dim * w.block_size))
+            st = buf.astype(np.int64)
+            t0 = st[:, 1][st[:, 1] > 0].min()
+            raw.append({"pages": st[:, 8].astype(float), "segments": st[:, 9].astype(float),
+                        **{name: np.where(st[:, i] > 0, (st[:, i] - t0) / 1e3, np.nan)
+                           for i, name in enumerate(STAMP_NAMES)}})
     keys = [k for k in per[0] if isinstance(per[0][k], float)]
     summary = {k: float(np.median([d[k] for d in per])) for k in keys}
     summary["ctas_with_work"] = per[0]["ctas_with_work"]
     summary["pages_per_cta_min_max"] = per[0]["pages_per_cta_min_max"]
-    return {"stamps": summary, "samples": len(per), "workload": args.workload,
+    line = {"stamps": summary, "samples": len(per), "workload": args.workload,
             "kv_bytes_per_step": w.kv_bytes,
             "note": "medians over samples; times in us from the first CTA past the wait for "
                     "the previous kernels; steady_gbs = sum over CTAs of pages x 4096 B over "
                     "(pages done - first pages)"}
+    if args.stamps_per_cta:  # per CTA, median over samples: pages, segments, phase times (us)
+        line["per_cta"] = {k: np.nanmedian(np.stack([d[k] for d in raw]), axis=0).round(3).tolist()
+                           for k in raw[0]}
+    return line
 
 
 # --------------------------------------------------------------------------
@@ -777,6 +786,8 @@ def main(argv=None):
                     help="print the partial kernel's phase breakdown from the timestamped "
                          "diagnostic build instead of a bench line")
     ap.add_argument("--stamp-samples", type=int, default=50)
+    ap.add_argument("--stamps-per-cta", action="store_true",
+                    help="with --stamps: also print every CTA's pages and phase times")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         raise SystemExit("--steps must be >= 1 and --warmup >= 0")

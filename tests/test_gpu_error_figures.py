@@ -4,11 +4,11 @@ The stated bound is max abs error 2e-3 and max rel error 1e-2 on the fp16
 outputs against the float64 oracle. The parity tests apply it element by
 element as |gpu - ref| <= 2e-3 + 1e-2*|ref|; here the two figures are also
 measured separately: max abs over all elements, max rel over the elements
-with |ref| > 2e-3. Where the outputs are O(1) (tiny, B4, B8, B16), fp16
-rounding of the output (<= 2^-11 relative) leaves room for the abs bound on
-its own, and it is asserted outright. The boundary workload's outputs reach
-|out| = 14, where one fp16 rounding step alone is 3.9e-3: there only the
-combined bound can hold.
+with |ref| > 2e-3. The outputs of all five workloads stay below 4 in
+magnitude, where one fp16 rounding step is at most 9.8e-4, so the abs bound
+is asserted outright for every workload and format. Max rel is reported, not
+asserted: next to |ref| = 2e-3 the rounding of the softmax weights to fp16
+alone can reach 1e-2 of the output.
 
 Run with ``-s`` to see the table; with XQA_ERROR_TABLE=<path> it is also
 written to that file.
@@ -24,8 +24,6 @@ from paged_fp8_kv_gqa_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-ABS_ONLY = {"tiny_b1_ctx256", "b4_uniform_ctx1024", "b8_uniform_ctx16384",
-            "b16_ragged_ctx16384_19200"}
 _ROWS = []
 
 
@@ -41,8 +39,7 @@ def test_error_figures(name, kv_dtype):
     ref = oracle_of(w)
     got = run(w)
     stats = assert_close(got, ref, f"{name} {kv_dtype}")  # the combined bound, every element
-    if name in ABS_ONLY:
-        assert stats["max_abs"] <= ATOL, (name, kv_dtype, stats)
+    assert stats["max_abs"] <= ATOL, (name, kv_dtype, stats)
     _ROWS.append((name, kv_dtype, stats["max_abs"], stats["max_rel"],
                   float(np.abs(ref).max())))
 
@@ -50,7 +47,7 @@ def test_error_figures(name, kv_dtype):
 def test_zz_print_error_table():
     if not _ROWS:
         pytest.skip("no figures collected in this run")
-    lines = ["| workload | format | max abs | max rel (|ref| > 2e-3) | max |ref| |",
+    lines = ["| workload | format | max abs | max rel (abs(ref) > 2e-3) | max abs(ref) |",
              "|---|---|---|---|---|"]
     for name, fmt, a, r, m in _ROWS:
         lines.append(f"| {name} | {fmt} | {a:.3e} | {r:.3e} | {m:.3g} |")
