@@ -551,10 +551,13 @@ def run_gpu(args, world, rank, local, dist):
 
 STAMP_NAMES = ("entry", "inputs_readable", "range_known", "first_pages", "pages_done",
                "merges_buffered", "tickets_taken", "exit")
+STAMPS_PER_CTA = 16  # the eight times above, pages, segments, six more times
+EXTRA_STAMPS = {10: "lengths_loaded", 11: "block_ids_loaded", 12: "all_warps_past_wait",
+                13: "plan_done", 14: "page_loop_entered", 15: "first_search_done"}
 
 
 def stamp_breakdown(st, page_bytes: int):
-    """Phases of one launch from its per-CTA stamps (int [ctas, 10]: eight
+    """Phases of one launch from its per-CTA stamps (int [ctas, >= 10]: eight
     %globaltimer values in ns, then the CTA's pages and segments). Times in
     us, relative to the moment the launch could read its inputs (the first
     CTA past the wait for the previous kernels)."""
@@ -584,6 +587,21 @@ def stamp_breakdown(st, page_bytes: int):
     }
 
 
+def stamp_columns(st):
+    """Per-CTA columns of one launch's stamps: pages, segments, and every
+    stamped time in us from the first CTA past the wait (NaN where unset)."""
+    import numpy as np
+
+    st = np.asarray(st, dtype=np.int64)
+    t0 = st[:, 1][st[:, 1] > 0].min()
+    names = {**dict(enumerate(STAMP_NAMES)), **EXTRA_STAMPS}
+    cols = {"pages": st[:, 8].astype(float), "segments": st[:, 9].astype(float)}
+    for i, name in names.items():
+        if i < st.shape[1]:
+            cols[name] = np.where(st[:, i] > 0, (st[:, i] - t0) / 1e3, np.nan)
+    return cols
+
+
 def run_stamps(args):
     """Phase breakdown of the partial kernel from the timestamped diagnostic
     build (never the headline: its numbers come from the library as built).
@@ -602,7 +620,8 @@ def run_stamps(args):
     from paged_fp8_kv_gqa_gb300 import build as _build
 
     xqa._lib = None
-    xqa.LIB_PATH = _build.build(variant="stamps")
+    # a differently built stamped library with the same ABI (A/B of phases), else this tree's
+    xqa.LIB_PATH = os.path.abspath(args.lib) if args.lib else _build.build(variant="stamps")
     lib = xqa.load_library()
     lib.xqa_diag_read_stamps.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
     lib.xqa_diag_read_stamps.restype = ctypes.c_int
@@ -627,7 +646,7 @@ def run_stamps(args):
             step(0)
             step(1)
     per, raw = [], []
-    buf = np.zeros((n_ctas, 10), np.uint64)
+    buf = np.zeros((n_ctas, STAMPS_PER_CTA), np.uint64)
     for r in range(args.stamp_samples + 5):
         with torch.cuda.stream(stream):
             g.replay()
@@ -637,11 +656,7 @@ def run_stamps(args):
             raise RuntimeError(f"xqa_diag_read_stamps: status {rc}")
         if r >= 5:
             per.append(stamp_breakdown(buf.copy(), 2 * w.head_dim * w.block_size))
-            st = buf.astype(np.int64)
-            t0 = st[:, 1][st[:, 1] > 0].min()
-            raw.append({"pages": st[:, 8].astype(float), "segments": st[:, 9].astype(float),
-                        **{name: np.where(st[:, i] > 0, (st[:, i] - t0) / 1e3, np.nan)
-                           for i, name in enumerate(STAMP_NAMES)}})
+            raw.append(stamp_columns(buf))
     keys = [k for k in per[0] if isinstance(per[0][k], float)]
     summary = {k: float(np.median([d[k] for d in per])) for k in keys}
     summary["ctas_with_work"] = per[0]["ctas_with_work"]
@@ -651,6 +666,13 @@ def run_stamps(args):
             "note": "medians over samples; times in us from the first CTA past the wait for "
                     "the previous kernels; steady_gbs = sum over CTAs of pages x 4096 B over "
                     "(pages done - first pages)"}
+    # the CTA that exits last in each sample: its index, pages, segments and phase times
+    last = []
+    for cols in raw:
+        i = int(np.nanargmax(cols["exit"]))
+        last.append({k: float(v[i]) for k, v in cols.items()} | {"cta": i})
+    line["last_exit"] = {k: float(np.median([d[k] for d in last])) for k in last[0]}
+    line["last_exit"]["ctas_seen"] = sorted({d["cta"] for d in last})[:20]
     if args.stamps_per_cta:  # per CTA, median over samples: pages, segments, phase times (us)
         line["per_cta"] = {k: np.nanmedian(np.stack([d[k] for d in raw]), axis=0).round(3).tolist()
                            for k in raw[0]}

@@ -90,8 +90,11 @@ constexpr unsigned kFull = 0xffffffffu;
 //   3 first pages in warp 0's registers
 //   4 every warp done with its pages      5 buffered merges written
 //   6 merge tickets taken                 7 exit
-// and two counts: 8 the CTA's pages, 9 the segments its range touches.
-constexpr int kStampsPerCta = 10;
+// and two counts: 8 the CTA's pages, 9 the segments its range touches; then
+//   10 context lengths in registers   11 first block ids in registers
+//   12 every warp past the wait       13 plan done (before the range search)
+//   14 page loop entered              15 first segment search done
+constexpr int kStampsPerCta = 16;
 #ifdef XQA_STAMPS
 __device__ unsigned long long g_stamps[kMaxCtas * kStampsPerCta];
 __device__ __forceinline__ void stamp(int i) {
@@ -100,9 +103,17 @@ __device__ __forceinline__ void stamp(int i) {
 __device__ __forceinline__ void stamp_count(int i, int v) {
   if (threadIdx.x == 0) g_stamps[blockIdx.x * kStampsPerCta + i] = (unsigned long long)v;
 }
+// the time once v (a load's result) is in thread 0's registers
+__device__ __forceinline__ void stamp_after(int i, int v) {
+  if (threadIdx.x == 0) {
+    asm volatile("" ::"r"(v));
+    g_stamps[blockIdx.x * kStampsPerCta + i] = global_timer_ns();
+  }
+}
 #else
 __device__ __forceinline__ void stamp(int) {}
 __device__ __forceinline__ void stamp_count(int, int) {}
+__device__ __forceinline__ void stamp_after(int, int) {}
 #endif
 
 namespace {
@@ -138,6 +149,7 @@ __device__ __forceinline__ PageBatch load_batch(const PartialParams& p, const in
   if (q < npages) {
     const int pg = cbeg + q;
     const int s = find_segment(segs, s_first, nseg, pg);
+    if (base == 0) stamp_after(15, s);
     const int b = s / p.num_kv_heads, kvh = s - b * p.num_kv_heads;
     const int j = pg - segs[s];
     const int id = __ldg(&p.block_tables[(size_t)b * p.max_blocks_per_seq + j]);
@@ -606,6 +618,7 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
   stamp(1);
   if (cta == 0 && tid == 0) p.header[0] = gridDim.x;  // status words this call writes
   __syncthreads();
+  stamp(12);
   if (segs_in_smem) {
     const long long max_ctx = (long long)p.max_blocks_per_seq * kBlockSize;
     for (int base = 0; base < p.batch; base += kThreads) {
@@ -613,6 +626,7 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
       int pages = 0;
       if (b < p.batch) {
         const int ctx = __ldg(&p.context_lens[b]);
+        if (base == 0) stamp_after(10, ctx);
         sm.ctx_cache[b] = ctx;
         pages = (ctx < 0 || (long long)ctx > max_ctx) ? 0 : (ctx + kBlockSize - 1) / kBlockSize;
       }
@@ -697,6 +711,7 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
     }
   }
   if (cta >= n) return false;
+  stamp(13);
   // This CTA's positions [vlo, vhi) on the cost line, and the pages there: the
   // first page at a position >= a lies in the first segment whose pages end
   // past a. One parallel pass over the segments finds both ends (and the
@@ -957,8 +972,10 @@ __device__ __forceinline__ void cta_mode_range(const PartialParams& p, const CUt
 
   // ---- this warp's loads: owned page k is CTA-local page warp + 8k ----
   const int owned = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
+  stamp(14);
   PageBatch cur = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 0, lane);
   PageBatch nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 32, lane);
+  stamp_after(11, cur.y ^ nxt.y);
   int cur_base = 0;
   auto issue_next = [&]() {
     if (issued >= owned) return;

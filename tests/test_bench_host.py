@@ -76,3 +76,16 @@ def test_stamp_breakdown_on_synthetic_stamps():
     rate = 100 * 4096 / 40000 + 120 * 4096 / 41500  # bytes per ns = GB/s
     assert abs(b["steady_gbs"] - rate) < 1e-9
     assert b["pages_per_cta_min_max"] == [100, 120]
+
+
+def test_stamp_columns_per_cta():
+    st = np.zeros((2, 12), np.int64)
+    st[0, :8] = [500, 1000, 1500, 3000, 43000, 44000, 45000, 46000]
+    st[0, 8:] = [100, 1, 1200, 2000]
+    st[1, :8] = [600, 1100, 0, 0, 0, 0, 0, 1300]
+    c = bench.stamp_columns(st)
+    assert c["pages"].tolist() == [100, 0] and c["segments"].tolist() == [1, 0]
+    assert c["exit"].tolist() == [45.0, 0.3]
+    assert c["lengths_loaded"][0] == 0.2 and np.isnan(c["lengths_loaded"][1])
+    assert c["block_ids_loaded"][0] == 1.0
+    assert np.isnan(c["range_known"][1])
