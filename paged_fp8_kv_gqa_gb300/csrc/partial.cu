@@ -383,20 +383,24 @@ __device__ __forceinline__ void store_half4(__half* o, float a, float b, float c
 
 // LSE merge of the split segments this CTA completed (at most two: the first
 // and the last of its range) into fp16 rows, thread: column col, dims
-// dq..dq+3. Pieces were written by other CTAs: read through L2. The bad flags
-// (known from the merge tickets) and, for segments of at most kFew pieces,
-// every piece of both segments are loaded before any is used (one round trip
-// for the whole merge); in one-tile
-// kernels a segment of up to 16 pieces takes one round trip of its own, a
-// longer one two per 16 (two-tile kernels, short of registers: the maxima 16
-// and the sums 8 pieces per round trip).
+// dq..dq+3 (col is uniform over a warp). Pieces were written by other CTAs:
+// read through L2. The bad flags come from the merge tickets. For segments of
+// at most kFew pieces, every piece of both segments is loaded before any is
+// used (one round trip for the whole merge). In one-tile kernels a segment of
+// up to 16 pieces takes one round trip of its own: lane k loads piece k's
+// maximum and sum and the warp shares them by shuffles, so a lane holds only
+// its dims of each piece's O (fewer registers, so every load of the batch
+// stays in flight). Longer segments, and two-tile kernels (short of
+// registers), take the maxima 16 per round trip, then the sums 16 or 8. The
+// sums always run in piece order with the combine kernel's arithmetic
+// (bitwise equal results).
 template <bool kWide>  // one round trip for up to 16 pieces (else 8, fewer registers)
 __device__ __forceinline__ void merge_segments(const PartialParams& p, const int (&ms)[2],
                                                const int (&mbad)[2], int nm, const int32_t* segs,
                                                const int32_t* cc, long long line, int n, int col,
                                                int dq, float v_scale) {
   if (col >= p.group * p.q_len) return;
-  constexpr int kFew = 4;
+  constexpr int kFew = 6;  // 6 covers the 5-6 pieces of 16K-token segments on 152 SMs
   int ilo[2], ihi[2], bad[2];
   float mi[2][kFew], li[2][kFew];
   float4 oi[2][kFew];
@@ -409,7 +413,7 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
       bad[j] = mbad[j];
 #pragma unroll
       for (int k = 0; k < kFew; ++k) {
-        if (ilo[j] + k <= ihi[j]) {
+        if (ilo[j] + k <= ihi[j] && ihi[j] - ilo[j] < kFew) {  // larger segments load their own batch
           const float* slot = p.partials + (size_t)(ilo[j] + k + s) * kSlotFloats;
           mi[j][k] = __ldcg(slot + kSlotM + col);
           li[j][k] = __ldcg(slot + kSlotL + col);
@@ -447,25 +451,30 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
         }
       }
     } else if (kWide && ihi[j] - ilo[j] < 16) {  // up to 16 pieces: still one round trip
-      float mb[16], lb[16];
+      // lane k loads piece k's maximum and sum; the warp shares them by shuffles
+      const int lane = threadIdx.x & 31, np = ihi[j] - ilo[j] + 1;
+      float mk = -INFINITY, lk = 0.f;
+      if (lane < np) {
+        const float* slot = p.partials + (size_t)(ilo[j] + lane + s) * kSlotFloats;
+        mk = __ldcg(slot + kSlotM + col);
+        lk = __ldcg(slot + kSlotL + col);
+      }
       float4 ob[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if (ilo[j] + k <= ihi[j]) {
-          const float* slot = p.partials + (size_t)(ilo[j] + k + s) * kSlotFloats;
-          mb[k] = __ldcg(slot + kSlotM + col);
-          lb[k] = __ldcg(slot + kSlotL + col);
-          ob[k] = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
-        }
-      }
-#pragma unroll
       for (int k = 0; k < 16; ++k)
-        if (ilo[j] + k <= ihi[j]) M = fmaxf(M, mb[k]);
+        if (k < np)
+          ob[k] = __ldcg(reinterpret_cast<const float4*>(p.partials + (size_t)(ilo[j] + k + s) * kSlotFloats +
+                                                         col * kHeadDim + dq));
+      float mx = mk;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+      M = mx;
+      const float wk = (mk == -INFINITY) ? 0.f : ex2(mk - M);
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        if (ilo[j] + k <= ihi[j]) {
-          const float w = (mb[k] == -INFINITY) ? 0.f : ex2(mb[k] - M);
-          L += w * lb[k];
+        if (k < np) {
+          const float w = __shfl_sync(kFull, wk, k), l = __shfl_sync(kFull, lk, k);
+          L += w * l;
           acc.x += w * ob[k].x;
           acc.y += w * ob[k].y;
           acc.z += w * ob[k].z;
