@@ -551,9 +551,10 @@ def run_gpu(args, world, rank, local, dist):
 
 STAMP_NAMES = ("entry", "inputs_readable", "range_known", "first_pages", "pages_done",
                "merges_buffered", "tickets_taken", "exit")
-STAMPS_PER_CTA = 16  # the eight times above, pages, segments, six more times
+STAMPS_PER_CTA = 18  # the eight times above, pages, segments, eight more times
 EXTRA_STAMPS = {10: "lengths_loaded", 11: "block_ids_loaded", 12: "all_warps_past_wait",
-                13: "plan_done", 14: "page_loop_entered", 15: "first_search_done"}
+                13: "plan_done", 14: "page_loop_entered", 15: "first_search_done",
+                16: "merge_range_known", 17: "merge_loads_in"}
 
 
 def stamp_breakdown(st, page_bytes: int):

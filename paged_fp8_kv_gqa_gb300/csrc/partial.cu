@@ -94,7 +94,8 @@ constexpr unsigned kFull = 0xffffffffu;
 //   10 context lengths in registers   11 first block ids in registers
 //   12 every warp past the wait       13 plan done (before the range search)
 //   14 page loop entered              15 first segment search done
-constexpr int kStampsPerCta = 16;
+//   16 final merge: piece range known 17 final merge: first segment's loads in
+constexpr int kStampsPerCta = 18;
 #ifdef XQA_STAMPS
 __device__ unsigned long long g_stamps[kMaxCtas * kStampsPerCta];
 __device__ __forceinline__ void stamp(int i) {
@@ -396,9 +397,9 @@ __device__ __forceinline__ void store_half4(__half* o, float a, float b, float c
 // (bitwise equal results).
 template <bool kWide>  // one round trip for up to 16 pieces (else 8, fewer registers)
 __device__ __forceinline__ void merge_segments(const PartialParams& p, const int (&ms)[2],
-                                               const int (&mbad)[2], int nm, const int32_t* segs,
-                                               const int32_t* cc, long long line, int n, int col,
-                                               int dq, float v_scale) {
+                                               const int (&mbad)[2], const int (&milo)[2],
+                                               const int (&mihi)[2], int nm, int col, int dq,
+                                               float v_scale) {
   if (col >= p.group * p.q_len) return;
   constexpr int kFew = 6;  // 6 covers the 5-6 pieces of 16K-token segments on 152 SMs
   int ilo[2], ihi[2], bad[2];
@@ -408,8 +409,9 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
   for (int j = 0; j < 2; ++j) {
     if (j < nm) {
       const int s = ms[j];
-      ilo[j] = cta_of_vpos((long long)segs[s] + cc[s], line, n);
-      ihi[j] = cta_of_vpos((long long)segs[s + 1] - 1 + cc[s], line, n);
+      ilo[j] = milo[j];
+      ihi[j] = mihi[j];
+      if (j == 0) stamp_after(16, ihi[j] - ilo[j]);
       bad[j] = mbad[j];
 #pragma unroll
       for (int k = 0; k < kFew; ++k) {
@@ -465,6 +467,7 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
         if (k < np)
           ob[k] = __ldcg(reinterpret_cast<const float4*>(p.partials + (size_t)(ilo[j] + k + s) * kSlotFloats +
                                                          col * kHeadDim + dq));
+      if (j == 0) stamp_after(17, __float_as_int(ob[0].x) ^ __float_as_int(lk));
       float mx = mk;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
@@ -537,13 +540,15 @@ struct CtaShared {
   int abort_flag;              // a wait ran out of time: stop issuing, drain
   int scan_warp[kWarps], scan_warp_cost[kWarps];
   int scan_carry, scan_carry_cost;
-  long long cost_line;  // kept here: the end of the kernel reads it back
+  long long cost_line;  // the line's length, for piece_owners
   int range_lo, range_hi, range_seg, range_seg_hi;  // pages; first, last segment
-  const int32_t* cc_base;  // the cost-line prefix the end of the kernel reads
   // split pieces of this CTA (at most its first and last segment), whose
   // merge tickets are taken once the whole range is done
   int pend_seg[2], pend_poison[2], pend_last[2], pend_bad[2];
   int npend;
+  // the range's first and last segment (the only ones a range can share with
+  // other CTAs) and the CTAs holding their first and last page
+  int own_seg[2], own_ilo[2], own_ihi[2];
   int cta_status;  // first error this CTA met (XQA_OK if none), published at exit
 #ifdef XQA_STAMPS
   int first_stamped;
@@ -780,11 +785,27 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
   }
   rv.segs = segs;
   rv.cc = cc;
-  if (tid == 0) sh.cc_base = cc;
   stamp(2);
   stamp_count(8, rv.npages);
   stamp_count(9, sh.range_seg_hi - rv.s_first + 1);
   return true;
+}
+
+// One thread, once the range's first pages are in flight: the CTAs holding the
+// first and the last page of the range's first and last segment (two 64-bit
+// divisions each), which the end of the range needs for the merge tickets and
+// the final merge and would otherwise compute on its critical path.
+template <int NT>
+__device__ __forceinline__ void piece_owners(CtaShared<NT>& sh, const RangeView& rv) {
+  const long long line = sh.cost_line;
+  const int s_last = find_segment(rv.segs, rv.s_first, rv.s_hi + 1, rv.cend - 1);
+#pragma unroll 1
+  for (int e = 0; e < 2; ++e) {
+    const int sg = e == 0 ? rv.s_first : s_last;
+    sh.own_seg[e] = sg;
+    sh.own_ilo[e] = cta_of_vpos((long long)rv.segs[sg] + rv.cc[sg], line, rv.n);
+    sh.own_ihi[e] = cta_of_vpos((long long)rv.segs[sg + 1] - 1 + rv.cc[sg], line, rv.n);
+  }
 }
 
 // Lane 0 of a warp: the two TMA loads (K and V slice of one page) into ring
@@ -1004,6 +1025,7 @@ __device__ __forceinline__ void cta_mode_range(const PartialParams& p, const CUt
   };
 #pragma unroll 1
   for (int i = 0; i < kLookahead; ++i) issue_next();
+  if (warp == kWarps - 1 && lane == 0) piece_owners<NT>(sh, rv);
 
   int s = s_first;
   int q0 = 0;
@@ -1110,11 +1132,6 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
 
   const int npend = sh.npend;
   if (npend > 0) {
-    // the cost line again, read back rather than kept live through the loop
-    const int32_t* cc = sh.cc_base;
-    const long long line = *reinterpret_cast<volatile long long*>(&sh.cost_line);
-    const int32_t* segs = rv.segs;
-    const int n = rv.n;
     consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
     if (tid < npend) {
       // A split segment's ticket is the word of the CTA holding its first page
@@ -1123,8 +1140,8 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
       // the last, learns from the same atomic whether any piece was bad, and
       // clears the word for the next call (every other piece has added to it).
       const int ps = sh.pend_seg[tid];
-      const int ilo = cta_of_vpos((long long)segs[ps] + cc[ps], line, n);
-      const int ihi = cta_of_vpos((long long)segs[ps + 1] - 1 + cc[ps], line, n);
+      const int e = ps == sh.own_seg[0] ? 0 : 1;  // a split piece is the range's first or last
+      const int ilo = sh.own_ilo[e], ihi = sh.own_ihi[e];
       const int add = 1 + (sh.pend_poison[tid] ? kTicketPoison : 0);
       int last = 0, bad = 0;
       if (p.fused_merge) {
@@ -1158,9 +1175,11 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
       ++nm;
     }
     const int ms[2] = {m0, m1}, mbad[2] = {b0, b1};
+    const int e0 = m0 == sh.own_seg[0] ? 0 : 1, e1 = m1 == sh.own_seg[0] ? 0 : 1;
+    const int milo[2] = {sh.own_ilo[e0], sh.own_ilo[e1]}, mihi[2] = {sh.own_ihi[e0], sh.own_ihi[e1]};
     if (nm > 0)
       for (int col = tid >> 5; col < kCols; col += kWarps)
-        merge_segments<NT == 1>(p, ms, mbad, nm, segs, cc, line, n, col, (tid & 31) * 4, v_scale);
+        merge_segments<NT == 1>(p, ms, mbad, milo, mihi, nm, col, (tid & 31) * 4, v_scale);
   }
 
   // Drain: after an abort some issued copies may not have been waited for.
@@ -1348,6 +1367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 #pragma unroll 1
     for (int i = 0; i < kLookahead; ++i) issue_next_w();
+    if (warp == kWarps - 1 && lane == 0) piece_owners<NT>(sh, rv);
 
     int k = 0;  // this warp's running page index (ring slot and phase)
     for (int j = next_piece(warp); j < nsr; j = next_piece(j + kWarps)) {
