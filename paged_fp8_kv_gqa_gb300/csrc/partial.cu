@@ -731,7 +731,17 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
   // past a. One parallel pass over the segments finds both ends (and the
   // first segment) in shared memory, in place of two dependent searches.
   const long long line = (long long)total + (nseg > 0 ? cc[nseg - 1] : 0);
-  const long long vlo = ((long long)cta * line) / n, vhi = ((long long)(cta + 1) * line) / n;
+  long long vlo, vhi;  // floor(cta * line / n), floor((cta + 1) * line / n)
+  if (line <= 0xffffffffll) {
+    // exact in 32 bits: line = q n + r, so cta line / n = cta q + cta r / n
+    // with cta r < n^2 <= 2^20 (a 64-bit division is a long software routine)
+    const uint32_t q = (uint32_t)line / (uint32_t)n, r = (uint32_t)line - q * (uint32_t)n;
+    vlo = (long long)((uint32_t)cta * q + ((uint32_t)cta * r) / (uint32_t)n);
+    vhi = (long long)((uint32_t)(cta + 1) * q + ((uint32_t)(cta + 1) * r) / (uint32_t)n);
+  } else {
+    vlo = ((long long)cta * line) / n;
+    vhi = ((long long)(cta + 1) * line) / n;
+  }
   if (tid == 0) {
     sh.cost_line = line;
     sh.range_lo = sh.range_hi = total;  // no segment ends past the position
