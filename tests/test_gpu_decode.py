@@ -396,3 +396,14 @@ def test_context_longer_than_table_is_reported(merge_mode):
     d.lens.copy_(to_dev(w.context_lens))
     d.run()
     assert d.status() == xqa.XQA_ERR_CTX_TOO_LONG
+
+
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_group16_split_segments(merge_mode):
+    # G = 16 (64 q heads / 4 kv heads) fills both 8-column MMA tiles for a
+    # single new token; long contexts over few CTAs split every segment
+    w = wl.make_custom([3000, 5000, 17, 1, 900], 64, 4, seed=91)
+    a = run(w, max_ctas=23, merge_mode=merge_mode)
+    assert_close(a, oracle_of(w), "G=16")
+    b = run(wl.to_nhd(w), max_ctas=23, merge_mode=merge_mode)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
