@@ -94,3 +94,29 @@ def test_warp_mode_bad_block_id_is_contained(merge_mode):
     assert np.all(np.isnan(out[bad].astype(np.float32)))
     good = [b for b in range(w.batch) if b != bad]
     assert_close(out[good], ref[good], "rows beside a bad block id (warp mode)")
+
+
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_warp_mode_leaves_the_tickets_at_zero(merge_mode):
+    # split pieces in warp mode take the same self-clearing merge tickets as in
+    # CTA mode; after good and bad calls the ticket words must be zero again
+    w = _short_batch(114)
+    assert _warp_mode_share(w) > 0.5
+    ref = oracle_of(w)
+    d = Dev(w, merge_mode=merge_mode)
+    for bad in (False, True, False):
+        if bad:
+            d.bt[11, 0] = w.num_blocks + 5
+        else:
+            d.bt.copy_(to_dev(w.block_tables))
+        d.run()
+        out = d.result()
+        torch.cuda.synchronize()
+        tickets = d.ws[64:64 + 4 * 1024].cpu().numpy().view(np.int32)
+        assert np.all(tickets == 0)
+        if bad:
+            assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
+            assert np.all(np.isnan(out[11].astype(np.float32)))
+        else:
+            assert d.status() == xqa.XQA_OK
+            assert_close(out, ref, "warp mode")
