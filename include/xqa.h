@@ -20,7 +20,8 @@
  *   - The library allocates no memory and reads no environment variables,
  *     never calls abort/exit and never synchronises except in the xqa_read_*
  *     helpers, which say so. Host state it keeps: a per-device "kernel
- *     attributes set" flag and the cached cuTensorMapEncodeTiled entry point.
+ *     attributes set" flag and SM count, and the cached cuTensorMapEncodeTiled
+ *     entry point.
  *     Device state it keeps: the XQA_STATIC_WORKSPACE_BYTES array of
  *     xqa_decode_static_workspace (one per device, shared by every call of
  *     that entry point). Between calls, a caller's workspace keeps the merge
@@ -56,7 +57,7 @@ typedef enum xqa_status {
   /* written by the device into the workspace status word: */
   XQA_ERR_BAD_BLOCK_ID = 16,    /* block_tables entry outside [0, num_blocks) */
   XQA_ERR_CTX_TOO_LONG = 17,    /* context length < 0 or > MBS * block_size */
-  XQA_ERR_DEVICE_TIMEOUT = 18,  /* a pipeline wait exceeded its time budget */
+  XQA_ERR_DEVICE_TIMEOUT = 18,  /* a pipeline or merge-ticket wait exceeded its time budget */
   XQA_ERR_DRAIN_TIMEOUT = 19    /* after a timeout, a copy was still in flight when its
                                    CTA exited: the device state is not to be trusted */
 } xqa_status_t;
@@ -84,9 +85,13 @@ typedef struct xqa_shape {
                                  values above 1024 are taken as 1024 */
   int32_t min_pages_per_cta;  /* planner lower bound on pages per CTA; 0 = 16 */
   int32_t merge_mode;         /* how segments split over several CTAs are merged:
-                                 0 = by the last CTA to finish one (inside the
-                                 partial kernel, default); 1 = by the separate
-                                 combine kernel (xqa_combine) */
+                                 0 = inside the partial kernel (default), by the
+                                 last CTA to finish one, or for a segment of
+                                 more than 16 pieces (6 when G * q_len > 8) by
+                                 its last CTAs to finish, each taking some of
+                                 the rows (when max_ctas <= SM count, so that
+                                 every CTA is resident at once);
+                                 1 = by the separate combine kernel (xqa_combine) */
   int32_t kv_dtype;           /* XQA_KV_E5M2 (0, default) or XQA_KV_E4M3 */
   int32_t kv_layout;          /* XQA_LAYOUT_HND (0, default) or XQA_LAYOUT_NHD */
   int32_t q_len;              /* T: new tokens per sequence; 0 or 1 = single-token
@@ -128,9 +133,10 @@ xqa_status_t xqa_kernels_per_call(const xqa_shape_t* shape, int32_t* kernels);
  *                 tickets at zero for the next. The tickets and status words
  *                 sit at fixed offsets, so one workspace may serve calls of
  *                 different shapes (sized for the largest). A call that is
- *                 not run to completion (or xqa_attend_partial with
- *                 merge_mode 1 not followed by xqa_combine) leaves it needing
- *                 a fresh zero fill
+ *                 not run to completion, or that reports
+ *                 XQA_ERR_DEVICE_TIMEOUT or XQA_ERR_DRAIN_TIMEOUT (or
+ *                 xqa_attend_partial with merge_mode 1 not followed by
+ *                 xqa_combine) leaves it needing a fresh zero fill
  *
  * out[b, h, :] = sum_t softmax_t(sm_scale * <q[b,h], k_t>) * v_t over the
  * ctx_b tokens of kv head h / G, rounded to fp16 (round to nearest even).

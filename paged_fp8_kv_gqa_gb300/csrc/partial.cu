@@ -382,26 +382,25 @@ __device__ __forceinline__ void store_half4(__half* o, float a, float b, float c
   *reinterpret_cast<uint2*>(o) = v;
 }
 
-// LSE merge of the split segments this CTA completed (at most two: the first
-// and the last of its range) into fp16 rows, thread: column col, dims
+// LSE merge of the split segments this CTA completed alone (at most two: the
+// first and the last of its range) into fp16 rows, thread: column col, dims
 // dq..dq+3 (col is uniform over a warp). Pieces were written by other CTAs:
-// read through L2. The bad flags come from the merge tickets. For segments of
-// at most kFew pieces, every piece of both segments is loaded before any is
-// used (one round trip for the whole merge). In one-tile kernels a segment of
-// up to 16 pieces takes one round trip of its own: lane k loads piece k's
+// read through L2. The bad flags come from the merge tickets (a bad segment
+// gets NaN rows whatever its piece count). For segments of at most kFew
+// pieces, every piece of both segments is loaded before any is used (one
+// round trip for the whole merge). In one-tile kernels a segment of up to
+// kWidePieces pieces takes one round trip of its own: lane k loads piece k's
 // maximum and sum and the warp shares them by shuffles, so a lane holds only
 // its dims of each piece's O (fewer registers, so every load of the batch
-// stays in flight). Longer segments, and two-tile kernels (short of
-// registers), take the maxima 16 per round trip, then the sums 16 or 8. The
-// sums always run in piece order with the combine kernel's arithmetic
-// (bitwise equal results).
-template <bool kWide>  // one round trip for up to 16 pieces (else 8, fewer registers)
+// stays in flight). Larger segments are merged by merge_staged. The sums run
+// in piece order with the combine kernel's arithmetic (bitwise equal results).
+template <bool kWide>  // one round trip for up to kWidePieces pieces (else kFewPieces)
 __device__ __forceinline__ void merge_segments(const PartialParams& p, const int (&ms)[2],
                                                const int (&mbad)[2], const int (&milo)[2],
                                                const int (&mihi)[2], int nm, int col, int dq,
                                                float v_scale) {
   if (col >= p.group * p.q_len) return;
-  constexpr int kFew = 6;  // 6 covers the 5-6 pieces of 16K-token segments on 152 SMs
+  constexpr int kFew = kFewPieces;
   int ilo[2], ihi[2], bad[2];
   float mi[2][kFew], li[2][kFew];
   float4 oi[2][kFew];
@@ -452,7 +451,7 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
           acc.w += w * oi[j][k].w;
         }
       }
-    } else if (kWide && ihi[j] - ilo[j] < 16) {  // up to 16 pieces: still one round trip
+    } else if (kWide && ihi[j] - ilo[j] < kWidePieces) {  // still one round trip
       // lane k loads piece k's maximum and sum; the warp shares them by shuffles
       const int lane = threadIdx.x & 31, np = ihi[j] - ilo[j] + 1;
       float mk = -INFINITY, lk = 0.f;
@@ -461,9 +460,9 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
         mk = __ldcg(slot + kSlotM + col);
         lk = __ldcg(slot + kSlotL + col);
       }
-      float4 ob[16];
+      float4 ob[kWidePieces];
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
+      for (int k = 0; k < kWidePieces; ++k)
         if (k < np)
           ob[k] = __ldcg(reinterpret_cast<const float4*>(p.partials + (size_t)(ilo[j] + k + s) * kSlotFloats +
                                                          col * kHeadDim + dq));
@@ -474,7 +473,7 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
       M = mx;
       const float wk = (mk == -INFINITY) ? 0.f : ex2(mk - M);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < kWidePieces; ++k) {
         if (k < np) {
           const float w = __shfl_sync(kFull, wk, k), l = __shfl_sync(kFull, lk, k);
           L += w * l;
@@ -482,42 +481,6 @@ __device__ __forceinline__ void merge_segments(const PartialParams& p, const int
           acc.y += w * ob[k].y;
           acc.z += w * ob[k].z;
           acc.w += w * ob[k].w;
-        }
-      }
-    } else {  // more: the maxima 16 per round trip, then the weighted sums
-      constexpr int kSum = kWide ? 16 : 8;  // pieces per round trip of the sums
-      for (int base = ilo[j]; base <= ihi[j]; base += 16) {
-        float mb[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          if (base + k <= ihi[j])
-            mb[k] = __ldcg(p.partials + (size_t)(base + k + s) * kSlotFloats + kSlotM + col);
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          if (base + k <= ihi[j]) M = fmaxf(M, mb[k]);
-      }
-      for (int base = ilo[j]; base <= ihi[j]; base += kSum) {
-        float mb[kSum], lb[kSum];
-        float4 ob[kSum];
-#pragma unroll
-        for (int k = 0; k < kSum; ++k) {
-          if (base + k <= ihi[j]) {
-            const float* slot = p.partials + (size_t)(base + k + s) * kSlotFloats;
-            mb[k] = __ldcg(slot + kSlotM + col);
-            lb[k] = __ldcg(slot + kSlotL + col);
-            ob[k] = __ldcg(reinterpret_cast<const float4*>(slot + col * kHeadDim + dq));
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < kSum; ++k) {
-          if (base + k <= ihi[j]) {
-            const float w = (mb[k] == -INFINITY) ? 0.f : ex2(mb[k] - M);
-            L += w * lb[k];
-            acc.x += w * ob[k].x;
-            acc.y += w * ob[k].y;
-            acc.z += w * ob[k].z;
-            acc.w += w * ob[k].w;
-          }
         }
       }
     }
@@ -545,6 +508,10 @@ struct CtaShared {
   // split pieces of this CTA (at most its first and last segment), whose
   // merge tickets are taken once the whole range is done
   int pend_seg[2], pend_poison[2], pend_last[2], pend_bad[2];
+  // pieces of segments merged by merge_shared: rank (-1: none; 0: the last
+  // piece), merging CTAs, and the ticket word after the piece's add
+  int pend_rank[2], pend_nh[2], pend_word[2];
+  int wait_word;  // the ticket word a helper saw complete (-1: it did not)
   int npend;
   // the range's first and last segment (the only ones a range can share with
   // other CTAs) and the CTAs holding their first and last page
@@ -1117,6 +1084,163 @@ __device__ __forceinline__ void cta_mode_range(const PartialParams& p, const CUt
   }
 }
 
+// Merge of the rows row0, row0 + rstride, ... (< G * q_len) of a good split
+// segment too large for merge_segments, by every thread of the CTA. The
+// pieces' rows and their (m, l) words are gathered into shared memory (the
+// page ring and the merge buffers, free once the range is done) by all 256
+// threads, kGatherLoads 16-byte loads in flight per thread, as many pieces per
+// batch as fit; then warp w sums the CTA's rows w and w + kWarps over the
+// pieces (lane: dims 4 * lane .. 4 * lane + 3). Each warp reads every
+// piece's maximum for its row with lane-parallel loads issued with the first
+// gather. The sums run in piece order with the combine kernel's arithmetic
+// (bitwise equal results).
+template <int NT>
+__device__ __forceinline__ void merge_staged(const PartialParams& p, uint8_t* stage, int s,
+                                             int ilo, int ihi, int row0, int rstride,
+                                             float v_scale) {
+  constexpr int kCap = kStages * kStageBytes +
+                       PartialGeom<NT>::kMergeBufs * PartialGeom<NT>::kMergeBufFloats * 4;
+  constexpr int kGatherLoads = 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, dq = lane * 4;
+  const int ncols = p.group * p.q_len;
+  const int nrows = (ncols - row0 + rstride - 1) / rstride;  // rows of this CTA (>= 1)
+  const int np = ihi - ilo + 1;
+  const int per = kCap / (nrows * (kHeadDim * 4 + 8));  // pieces per batch
+  const float* first = p.partials + (size_t)(ilo + s) * kSlotFloats;
+  stamp_after(16, np);
+  float M[NT], L[NT];
+  float4 acc[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    M[j] = -INFINITY;
+    L[j] = 0.f;
+    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int b0 = 0; b0 < np; b0 += per) {
+    const int nb = min(per, np - b0);
+    const int nchunks = nb * nrows * (kHeadDim / 4);  // 16-byte chunks: (piece, row, dims)
+    float* ml = reinterpret_cast<float*>(stage + (size_t)nchunks * 16);  // (piece, row): m, l
+    if (b0 > 0) __syncthreads();  // every warp is done with the previous batch
+    for (int rp = tid; rp < nb * nrows; rp += kThreads) {  // (piece, row) pairs
+      const int k = rp / nrows, i = rp - k * nrows;
+      const float* slot = first + (size_t)(b0 + k) * kSlotFloats;
+      ml[2 * rp] = __ldcg(slot + kSlotM + row0 + i * rstride);
+      ml[2 * rp + 1] = __ldcg(slot + kSlotL + row0 + i * rstride);
+    }
+    if (b0 == 0) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {  // the maximum over every piece, for this warp's row
+        const int i = warp + kWarps * j, col = row0 + i * rstride;
+        float mx = -INFINITY;
+        if (i < nrows) {
+          for (int base = 0; base < np; base += 128) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int k = base + 32 * u + lane;
+              v[u] = k < np ? __ldcg(first + (size_t)k * kSlotFloats + kSlotM + col) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) mx = fmaxf(mx, v[u]);
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+        }
+        M[j] = mx;
+      }
+    }
+    for (int c0 = 0; c0 < nchunks; c0 += kThreads * kGatherLoads) {
+      float4 v[kGatherLoads];
+#pragma unroll
+      for (int u = 0; u < kGatherLoads; ++u) {
+        const int c = c0 + u * kThreads + tid;
+        if (c < nchunks) {
+          const int rp = c >> 5, k = rp / nrows, i = rp - k * nrows;
+          v[u] = __ldcg(reinterpret_cast<const float4*>(
+              first + (size_t)(b0 + k) * kSlotFloats + (row0 + i * rstride) * kHeadDim + (c & 31) * 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherLoads; ++u) {
+        const int c = c0 + u * kThreads + tid;
+        if (c < nchunks) reinterpret_cast<float4*>(stage)[c] = v[u];
+      }
+    }
+    __syncthreads();
+    if (b0 == 0) stamp(17);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int i = warp + kWarps * j;
+      if (i >= nrows) continue;
+#pragma unroll 4
+      for (int k = 0; k < nb; ++k) {
+        const int rp = k * nrows + i;
+        const float mk = ml[2 * rp], lk = ml[2 * rp + 1];
+        const float4 o = reinterpret_cast<const float4*>(stage)[rp * 32 + lane];
+        const float w = (mk == -INFINITY) ? 0.f : ex2(mk - M[j]);
+        L[j] += w * lk;
+        acc[j].x += w * o.x;
+        acc[j].y += w * o.y;
+        acc[j].z += w * o.z;
+        acc[j].w += w * o.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int i = warp + kWarps * j, col = row0 + i * rstride;
+    if (i >= nrows) continue;
+    const float rr = (L[j] > 0.f) ? v_scale / L[j] : 0.f;  // a new token with no visible token: 0
+    store_half4(p.out + col_row(p, s, col) * kHeadDim + dq, acc[j].x * rr, acc[j].y * rr,
+                acc[j].z * rr, acc[j].w * rr);
+  }
+}
+
+// The final merges this CTA takes part in for segments of more than kAlone
+// pieces (at most two: its range's first and last segment), shared by each
+// segment's last nh pieces to arrive: the piece of rank r (0 = the last)
+// takes the rows r, r + nh, ... once every piece has arrived. The segments
+// this CTA completes come first, then those it helps with, which wait for
+// their last pieces. Each merging CTA adds kTicketRelease once it has seen
+// the complete count; the one that brings the releases to nh clears the word
+// for the next call. A CTA that aborted (its ring may still receive page
+// copies) writes NaN rows instead. Out of line: the code of the page loop
+// does not depend on it.
+template <int NT>
+__device__ __noinline__ void merge_shared(const PartialParams& p, CtaShared<NT>& sh,
+                                          uint8_t* stage, float v_scale) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int ncols = p.group * p.q_len;
+  const int npend = sh.npend;
+  const bool aborted = sh.abort_flag != 0;  // uniform: set only before the ticket barrier
+  for (int n = 0; n < 2 * npend; ++n) {
+    const int i = n % npend, rank = sh.pend_rank[i], s = sh.pend_seg[i];
+    if (rank < 0 || (rank == 0) != (n < npend)) continue;
+    const int e = s == sh.own_seg[0] ? 0 : 1;
+    const int ilo = sh.own_ilo[e], ihi = sh.own_ihi[e], nh = sh.pend_nh[i];
+    int word = sh.pend_word[i];
+    if (rank > 0) {  // wait until every piece has arrived
+      if (tid == 0) sh.wait_word = wait_ticket_count(&p.tickets[ilo], ihi - ilo + 1);
+      __syncthreads();
+      word = sh.wait_word;
+    }
+    const bool seen = word >= 0;  // -1: the count did not complete in time
+    int rel_old = 0;
+    if (nh > 1 && seen && tid == 0) rel_old = atomicAdd(&p.tickets[ilo], kTicketRelease);
+    if (!seen && tid == 0) record_status(&sh.cta_status, XQA_ERR_DEVICE_TIMEOUT);
+    if (seen && (word & kTicketPoisonMask) == 0 && !aborted) {
+      merge_staged<NT>(p, stage, s, ilo, ihi, rank, nh, v_scale);
+    } else {
+      for (int col = rank + nh * warp; col < ncols; col += nh * kWarps) {
+        const float nan = __int_as_float(0x7fc00000);
+        store_half4(p.out + col_row(p, s, col) * kHeadDim + (tid & 31) * 4, nan, nan, nan, nan);
+      }
+    }
+    if (nh > 1 && seen && tid == 0 && rel_old / kTicketRelease == nh - 1) p.tickets[ilo] = 0;
+    __syncthreads();  // the gathered rows and wait_word are read before they are written again
+  }
+}
+
 // End of a CTA's range: the merges still buffered (the range's last kBufs
 // segments, in order), then for each split piece its bad flag and merge
 // ticket, and the merge of every segment this CTA completes. The ticket (a
@@ -1131,6 +1255,7 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
                                              float v_scale, int issued, int kseg) {
   constexpr int kCols = PartialGeom<NT>::kCols;
   constexpr int kBufs = PartialGeom<NT>::kMergeBufs;
+  constexpr int kAlone = NT == 1 ? kWidePieces : kFewPieces;  // pieces the last merges alone
   const int tid = threadIdx.x, warp = tid >> 5;
   const int ncols = p.group * p.q_len;
   consumer_bar();
@@ -1146,20 +1271,29 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
     if (tid < npend) {
       // A split segment's ticket is the word of the CTA holding its first page
       // (unique in a call). Each piece adds 1, plus kTicketPoison if it met a
-      // bad page; the piece that brings the count to the number of pieces is
-      // the last, learns from the same atomic whether any piece was bad, and
-      // clears the word for the next call (every other piece has added to it).
+      // bad page; the old count is the piece's arrival order. The piece that
+      // brings the count to the number of pieces is the last and learns from
+      // the same atomic whether any piece was bad. A segment of at most
+      // kAlone pieces is merged by the last alone, which clears the word for
+      // the next call; a larger one by merge_shared.
       const int ps = sh.pend_seg[tid];
       const int e = ps == sh.own_seg[0] ? 0 : 1;  // a split piece is the range's first or last
       const int ilo = sh.own_ilo[e], ihi = sh.own_ihi[e];
       const int add = 1 + (sh.pend_poison[tid] ? kTicketPoison : 0);
-      int last = 0, bad = 0;
+      int last = 0, bad = 0, rank = -1;
       if (p.fused_merge) {
         // release: this CTA's slots (ordered before by the barrier) are visible
         // to whoever takes a later ticket; acquire: the earlier pieces are
         // visible to this CTA after the next barrier
         const int old = atom_add_acq_rel_gpu(&p.tickets[ilo], add);
-        if ((old & (kTicketPoison - 1)) == ihi - ilo) {
+        if (ihi - ilo >= kAlone) {
+          const int np = ihi - ilo + 1, r = np - 1 - (old & kTicketCountMask);
+          const int nh = max(1, min(min(np / 2, ncols), p.merge_helpers));
+          if (r < nh) rank = r;
+          if (r == 0 && nh == 1) p.tickets[ilo] = 0;
+          sh.pend_nh[tid] = nh;
+          sh.pend_word[tid] = old + add;  // complete for rank 0
+        } else if ((old & kTicketCountMask) == ihi - ilo) {
           last = 1;
           bad = (old >= kTicketPoison || add > 1) ? 1 : 0;
           p.tickets[ilo] = 0;
@@ -1169,10 +1303,11 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
       }
       sh.pend_last[tid] = last;
       sh.pend_bad[tid] = bad;
+      sh.pend_rank[tid] = rank;
     }
     consumer_bar();
     stamp(6);
-    int m0 = 0, m1 = 0, b0 = 0, b1 = 0, nm = 0;  // the segments this CTA completes (at most two)
+    int m0 = 0, m1 = 0, b0 = 0, b1 = 0, nm = 0;  // the segments this CTA completes alone
     for (int i = 0; i < npend; ++i) {
       if (!sh.pend_last[i]) continue;
       if (nm == 0) {
@@ -1190,6 +1325,10 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
     if (nm > 0)
       for (int col = tid >> 5; col < kCols; col += kWarps)
         merge_segments<NT == 1>(p, ms, mbad, milo, mihi, nm, col, (tid & 31) * 4, v_scale);
+    if (sh.pend_rank[0] >= 0 || (npend > 1 && sh.pend_rank[1] >= 0)) {
+      __syncthreads();  // the merge buffers and every warp's last pages are read
+      merge_shared<NT>(p, sh, sm.stages, v_scale);
+    }
   }
 
   // Drain: after an abort some issued copies may not have been waited for.

@@ -24,6 +24,7 @@ using xqa::kHeadDim;
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_attrs_set[kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];  // SM count, set with the attributes
 std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
 struct Resolved {
@@ -88,12 +89,23 @@ xqa_status_t check_workspace(const Resolved& r, const void* ws, size_t bytes) {
   return XQA_OK;
 }
 
+// SM count of the current device (cached by ensure_device_setup; 0 if unknown).
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return g_sms[dev].load(std::memory_order_acquire);
+}
+
 xqa_status_t ensure_device_setup() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return XQA_ERR_DEVICE;
   if (dev < 0 || dev >= kMaxDevices) return XQA_ERR_DEVICE;
   if (g_attrs_set[dev].load(std::memory_order_acquire) == 0) {
     if (xqa::set_partial_attributes() != cudaSuccess) return XQA_ERR_LAUNCH;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return XQA_ERR_DEVICE;
+    g_sms[dev].store(sms, std::memory_order_release);
     g_attrs_set[dev].store(1, std::memory_order_release);
   }
   if (g_encode.load(std::memory_order_acquire) == nullptr) {
@@ -215,6 +227,9 @@ xqa_status_t attend_partial_impl(const void* q, const uint8_t* k_cache, const ui
   p.n_max = r.n_max;
   p.min_pages = r.min_pages;
   p.fused_merge = r.merge_mode == 0 ? 1 : 0;
+  // CTAs that wait for one another's merge tickets need the whole grid
+  // resident at once: one CTA per SM, so no more CTAs than SMs
+  p.merge_helpers = r.n_max <= device_sms() ? xqa::kMergeHelpers : 1;
   p.batch = r.batch;
   p.num_q_heads = r.hq;
   p.num_kv_heads = r.hkv;

@@ -50,6 +50,12 @@ constexpr int kDefaultMinPagesPerCta = 16;
 // work that falls on CTAs holding segment boundaries; the value minimises the
 // step time of the B8, B16 and mixed-length workloads, swept over 0..48).
 constexpr int kSegCost = 32;
+// The final merge of a split segment by its last CTA alone, from registers:
+// up to kFewPieces pieces (both segments a CTA completes in one round trip),
+// or in one-tile kernels up to kWidePieces pieces (one round trip each).
+// Larger segments are merged by several CTAs, gathered in shared memory.
+constexpr int kFewPieces = 6;  // covers the 5-6 pieces of 16K-token segments on 152 SMs
+constexpr int kWidePieces = 16;
 // Warp mode of the partial kernel: a CTA range of at least this many segment
 // pieces, none longer than kWarpModePages pages, gives whole pieces to warps.
 constexpr int kWarpModeMinPieces = 4;
@@ -77,9 +83,20 @@ constexpr unsigned long long kWaitBudgetNs = 1000000000ull;  // 1 s
 // The merge-ticket and status regions below are sized by it, not by the
 // shape, so they sit at the same offsets whatever shape uses the workspace.
 constexpr int kMaxCtas = 1024;
-// A split segment's merge ticket counts its finished pieces in the low 16 bits
-// and its pieces that met a bad page in the high 16 bits.
+// A split segment's merge ticket counts its finished pieces in bits 0-15, its
+// pieces that met a bad page in bits 16-26 (at most kMaxCtas of them), and in
+// bits 27-30 the merging CTAs that have seen the count complete (when several
+// CTAs share the final merge).
 constexpr int kTicketPoison = 1 << 16;
+constexpr int kTicketRelease = 1 << 27;
+constexpr int kTicketCountMask = kTicketPoison - 1;
+constexpr int kTicketPoisonMask = kTicketRelease - kTicketPoison;
+static_assert(kMaxCtas * (long long)kTicketPoison < kTicketRelease, "poison bits overflow");
+// The final merge of a larger split segment is shared by up to this many of
+// its last CTAs (output rows dealt round robin) when every CTA of the launch
+// is resident at once.
+constexpr int kMergeHelpers = 8;
+static_assert(kMergeHelpers * (long long)kTicketRelease <= 0x7fffffffLL + 1, "release bits overflow");
 constexpr int kHeaderWords = 16;
 
 struct WsLayout {
@@ -294,6 +311,24 @@ __host__ __device__ inline int cta_of_vpos(long long v, long long line, long lon
   return (int)(((v + 1) * n - 1) / line);
 }
 
+
+// Device-scope load with acquire ordering.
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* addr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+// Polls a merge ticket (acquire) until its piece count reaches np; returns
+// the word, or -1 once kWaitBudgetNs have passed.
+__device__ __forceinline__ int wait_ticket_count(const int32_t* ticket, int np) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    const int w = ld_acquire_gpu(ticket);
+    if ((w & kTicketCountMask) == np) return w;
+    if (global_timer_ns() - t0 > kWaitBudgetNs) return -1;
+  }
+}
 
 // Device-scope fetch-and-add with acquire-release ordering.
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {

@@ -23,6 +23,8 @@ struct PartialParams {
   int q_len;                 // new tokens per sequence (q, out: [B, q_len, Hq, D])
   int n_max, min_pages;      // split rule inputs (same values the planner got)
   int fused_merge;           // 1: the last CTA of a split segment merges it
+  int merge_helpers;         // CTAs that may share a large segment's final merge (1: the
+                             // last alone; more only if every CTA is resident at once)
   int kv_dtype, kv_layout;   // XQA_KV_* code format, XQA_LAYOUT_* cache layout
   double qk_scale_base;      // sm_scale * log2(e); the logit scale is this * k_scale
   float k_scale, v_scale;    // per-tensor scales (used when the pointers are null)

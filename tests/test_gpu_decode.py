@@ -135,6 +135,18 @@ def test_one_long_sequence_split_over_every_cta(q_len):
     assert_close(a, ref, f"one 128K sequence, {q_len} new tokens")
 
 
+@pytest.mark.parametrize("hq,ctas", [(8, 300), (16, 300), (4, 1000)])
+def test_staged_merge_in_several_batches(hq, ctas):
+    # one sequence, one kv head, hundreds of CTAs: the final merge stages more
+    # pieces than fit in shared memory at once (47 per batch for G = 8, 24 for
+    # G = 16, 91 for G = 4), so it runs in several batches
+    w = wl.make_custom([32768], hq, 1, seed=64)
+    a = run(w, max_ctas=ctas, min_pages=1, merge_mode=0)
+    b = run(w, max_ctas=ctas, min_pages=1, merge_mode=1)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    assert_close(a, oracle_of(w), f"G={hq} over {ctas} CTAs")
+
+
 def test_single_token_context_is_the_v_row_by_value():
     w = wl.make_custom([1, 1, 1], 16, 2, seed=21, k_scale=0.5, v_scale=0.25)
     out = run(w)
@@ -237,6 +249,40 @@ def test_merge_tickets_are_zero_after_every_call(merge_mode):
     d.run()
     assert d.status() == xqa.XQA_OK
     assert_close(d.result(), ref, "after the bad calls")
+
+
+@pytest.mark.parametrize("hq,hkv,q_len", [(8, 1, 1), (16, 1, 1), (4, 1, 1), (8, 2, 2), (32, 4, 1)])
+def test_final_merge_shared_by_the_last_ctas(hq, hkv, q_len):
+    # long sequences over one CTA per SM: a segment of many pieces is merged by
+    # its last CTAs to finish, each taking every nh-th output row; results
+    # equal the combine kernel's bit for bit and the tickets end at zero
+    w = wl.make_custom([20000, 9000, 3], hq, hkv, seed=36, q_len=q_len)
+    d = Dev(w, merge_mode=0)
+    d.run()
+    a = d.result()
+    assert d.status() == xqa.XQA_OK
+    assert np.all(_tickets(d) == 0)
+    b = run(w, merge_mode=1)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    assert_close(a, oracle_of(w), f"shared final merge G={hq // hkv} q_len={q_len}")
+
+
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_bad_block_id_in_a_segment_merged_by_several_ctas(merge_mode):
+    w = wl.make_custom([20000, 300], 8, 1, seed=37)
+    ref = oracle_of(w)
+    d = Dev(w, merge_mode=merge_mode)
+    d.bt[0, 700] = w.num_blocks + 3
+    d.run()
+    assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
+    out = d.result()
+    assert np.all(np.isnan(out[0].astype(np.float32)))
+    assert_close(out[[1]], ref[[1]], "the sequence beside")
+    assert np.all(_tickets(d) == 0)
+    d.bt.copy_(to_dev(w.block_tables))
+    d.run()
+    assert d.status() == xqa.XQA_OK
+    assert_close(d.result(), ref, "after the bad call")
 
 
 def test_one_workspace_serves_several_shapes():
