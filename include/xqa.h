@@ -209,7 +209,7 @@ xqa_status_t xqa_selftest_wait_timeout(int32_t* device_status, uint64_t budget_n
 /* The device-reported status of the last call that used `workspace`:
  * *device_status receives XQA_OK or the first device-reported code in CTA
  * order (each CTA of the partial kernel writes its own status word as it
- * exits). Copies the fixed-size header/ticket/status region (8256 bytes) to
+ * exits). Copies the fixed-size header/ticket/status region (12352 bytes) to
  * the host and synchronises `stream`. Returns XQA_ERR_WORKSPACE if the
  * workspace holds no status (neither zero-filled nor written by a call). */
 xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void* stream);

@@ -509,8 +509,9 @@ struct CtaShared {
   // merge tickets are taken once the whole range is done
   int pend_seg[2], pend_poison[2], pend_last[2], pend_bad[2];
   // pieces of segments merged by merge_shared: rank (-1: none; 0: the last
-  // piece), merging CTAs, and the ticket word after the piece's add
-  int pend_rank[2], pend_nh[2], pend_word[2];
+  // piece to arrive) and merging CTAs
+  int pend_rank[2], pend_nh[2];
+  int arrived[2];  // old arrival counts of the range's first and last segment
   int wait_word;  // the ticket word a helper saw complete (-1: it did not)
   int npend;
   // the range's first and last segment (the only ones a range can share with
@@ -1199,13 +1200,14 @@ __device__ __forceinline__ void merge_staged(const PartialParams& p, uint8_t* st
 // The final merges this CTA takes part in for segments of more than kAlone
 // pieces (at most two: its range's first and last segment), shared by each
 // segment's last nh pieces to arrive: the piece of rank r (0 = the last)
-// takes the rows r, r + nh, ... once every piece has arrived. The segments
-// this CTA completes come first, then those it helps with, which wait for
-// their last pieces. Each merging CTA adds kTicketRelease once it has seen
-// the complete count; the one that brings the releases to nh clears the word
-// for the next call. A CTA that aborted (its ring may still receive page
-// copies) writes NaN rows instead. Out of line: the code of the page loop
-// does not depend on it.
+// takes the rows r, r + nh, ... once every piece is written (acquire through
+// the written count). The segments this CTA completes come first, then those
+// it helps with. Each merging CTA adds kTicketRelease to the arrival word
+// once it has seen every piece written; the one that brings the releases to
+// nh (or the last piece, when it merges alone) clears both words for the next
+// call. A CTA that aborted (its ring may still receive page copies) writes
+// NaN rows instead. Out of line: the code of the page loop does not depend
+// on it.
 template <int NT>
 __device__ __noinline__ void merge_shared(const PartialParams& p, CtaShared<NT>& sh,
                                           uint8_t* stage, float v_scale) {
@@ -1218,13 +1220,11 @@ __device__ __noinline__ void merge_shared(const PartialParams& p, CtaShared<NT>&
     if (rank < 0 || (rank == 0) != (n < npend)) continue;
     const int e = s == sh.own_seg[0] ? 0 : 1;
     const int ilo = sh.own_ilo[e], ihi = sh.own_ihi[e], nh = sh.pend_nh[i];
-    int word = sh.pend_word[i];
-    if (rank > 0) {  // wait until every piece has arrived
-      if (tid == 0) sh.wait_word = wait_ticket_count(&p.tickets[ilo], ihi - ilo + 1);
-      __syncthreads();
-      word = sh.wait_word;
-    }
-    const bool seen = word >= 0;  // -1: the count did not complete in time
+    int32_t* written = p.tickets + kMaxCtas + ilo;
+    if (tid == 0) sh.wait_word = wait_ticket_count(written, ihi - ilo + 1);
+    __syncthreads();
+    const int word = sh.wait_word;
+    const bool seen = word >= 0;  // -1: the pieces were not all written in time
     int rel_old = 0;
     if (nh > 1 && seen && tid == 0) rel_old = atomicAdd(&p.tickets[ilo], kTicketRelease);
     if (!seen && tid == 0) record_status(&sh.cta_status, XQA_ERR_DEVICE_TIMEOUT);
@@ -1236,7 +1236,10 @@ __device__ __noinline__ void merge_shared(const PartialParams& p, CtaShared<NT>&
         store_half4(p.out + col_row(p, s, col) * kHeadDim + (tid & 31) * 4, nan, nan, nan, nan);
       }
     }
-    if (nh > 1 && seen && tid == 0 && rel_old / kTicketRelease == nh - 1) p.tickets[ilo] = 0;
+    if (seen && tid == 0 && (nh == 1 || rel_old / kTicketRelease == nh - 1)) {
+      p.tickets[ilo] = 0;
+      *written = 0;
+    }
     __syncthreads();  // the gathered rows and wait_word are read before they are written again
   }
 }
@@ -1260,46 +1263,73 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
   const int ncols = p.group * p.q_len;
   consumer_bar();
   stamp(4);
+  // In-kernel merge: the arrival tickets of the range's split segments (its
+  // first and last; thread e takes segment e) are taken now, so that their
+  // round trip overlaps the merges of the buffered segments below.
+  int arrived = 0;
+  if (p.fused_merge && tid < 2 && (tid == 0 || sh.own_seg[1] != sh.own_seg[0]) &&
+      sh.own_ilo[tid] != sh.own_ihi[tid])
+    arrived = atomicAdd(&p.tickets[sh.own_ilo[tid]], 1);
   for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k)
     merge_buffer<NT>(p, sh, sm.merge_bufs, k % kBufs, ncols, v_scale);
+  if (tid < 2) sh.arrived[tid] = arrived;
   consumer_bar();
   stamp(5);
 
   const int npend = sh.npend;
   if (npend > 0) {
-    consumer_bar();  // all of this CTA's partial-slot writes precede the tickets
+    consumer_bar();  // all of this CTA's partial-slot writes precede the written counts
     if (tid < npend) {
-      // A split segment's ticket is the word of the CTA holding its first page
-      // (unique in a call). Each piece adds 1, plus kTicketPoison if it met a
-      // bad page; the old count is the piece's arrival order. The piece that
-      // brings the count to the number of pieces is the last and learns from
-      // the same atomic whether any piece was bad. A segment of at most
-      // kAlone pieces is merged by the last alone, which clears the word for
-      // the next call; a larger one by merge_shared.
+      // A split segment's tickets are the words of the CTA holding its first
+      // page (unique in a call). Each piece raises the written count by 1,
+      // plus kTicketPoison if it met a bad page, with release order after its
+      // slot. In-kernel merge, by the piece count:
+      //  * at most kFewPieces: the last piece to arrive (arrival rank 0)
+      //    merges alone once every other piece is written (acquire through
+      //    the written count; it does not raise it), then clears both words;
+      //  * up to kAlone: the piece that completes the written count (its
+      //    atomic returns the count and the bad flags) merges alone and
+      //    clears both words (the pieces' arrivals are close together here:
+      //    the last to arrive would often wait for another's slot);
+      //  * more: merge_shared, by the last nh pieces to arrive.
+      // Combine kernel: the first word takes the written counts; the combine
+      // kernel reads and clears it.
       const int ps = sh.pend_seg[tid];
       const int e = ps == sh.own_seg[0] ? 0 : 1;  // a split piece is the range's first or last
-      const int ilo = sh.own_ilo[e], ihi = sh.own_ihi[e];
+      const int ilo = sh.own_ilo[e], ihi = sh.own_ihi[e], np = ihi - ilo + 1;
       const int add = 1 + (sh.pend_poison[tid] ? kTicketPoison : 0);
+      int32_t* written = p.tickets + kMaxCtas + ilo;
       int last = 0, bad = 0, rank = -1;
       if (p.fused_merge) {
-        // release: this CTA's slots (ordered before by the barrier) are visible
-        // to whoever takes a later ticket; acquire: the earlier pieces are
-        // visible to this CTA after the next barrier
-        const int old = atom_add_acq_rel_gpu(&p.tickets[ilo], add);
-        if (ihi - ilo >= kAlone) {
-          const int np = ihi - ilo + 1, r = np - 1 - (old & kTicketCountMask);
+        const int r = np - 1 - (sh.arrived[e] & kTicketCountMask);
+        if (np > kAlone) {
           const int nh = max(1, min(min(np / 2, ncols), p.merge_helpers));
           if (r < nh) rank = r;
-          if (r == 0 && nh == 1) p.tickets[ilo] = 0;
+          red_add_release_gpu(written, add);
           sh.pend_nh[tid] = nh;
-          sh.pend_word[tid] = old + add;  // complete for rank 0
-        } else if ((old & kTicketCountMask) == ihi - ilo) {
+        } else if (np > kFewPieces) {
+          const int old = atom_add_acq_rel_gpu(written, add);
+          if ((old & kTicketCountMask) == np - 1) {
+            last = 1;
+            bad = ((old & kTicketPoisonMask) != 0 || add > 1) ? 1 : 0;
+            p.tickets[ilo] = 0;  // every piece arrived before raising the written count
+            *written = 0;
+          }
+        } else if (r == 0) {
+          const int w = wait_ticket_count(written, np - 1);  // the other pieces' slots
           last = 1;
-          bad = (old >= kTicketPoison || add > 1) ? 1 : 0;
-          p.tickets[ilo] = 0;
+          bad = (w < 0 || (w & kTicketPoisonMask) != 0 || add > 1) ? 1 : 0;
+          if (w < 0) {
+            record_status(&sh.cta_status, XQA_ERR_DEVICE_TIMEOUT);
+          } else {
+            p.tickets[ilo] = 0;
+            *written = 0;
+          }
+        } else {
+          red_add_release_gpu(written, add);
         }
       } else {
-        atomicAdd(&p.tickets[ilo], add);  // the combine kernel reads and clears it
+        red_add_release_gpu(&p.tickets[ilo], add);  // the combine kernel reads and clears it
       }
       sh.pend_last[tid] = last;
       sh.pend_bad[tid] = bad;

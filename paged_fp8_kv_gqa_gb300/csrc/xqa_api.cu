@@ -374,7 +374,7 @@ xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void
   // header, tickets and status words: one copy of a fixed-size region
   const xqa::WsLayout lay = xqa::ws_layout(0, 0);
   static_assert(xqa::kMaxCtas <= 1024, "status region copied through the stack");
-  int32_t words[xqa::kHeaderWords + 2 * xqa::kMaxCtas];
+  int32_t words[xqa::kHeaderWords + 3 * xqa::kMaxCtas];
   if (cudaMemcpyAsync(words, workspace, lay.seg_start_off, cudaMemcpyDeviceToHost, s) !=
           cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)

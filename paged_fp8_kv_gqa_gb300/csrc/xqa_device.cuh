@@ -83,10 +83,17 @@ constexpr unsigned long long kWaitBudgetNs = 1000000000ull;  // 1 s
 // The merge-ticket and status regions below are sized by it, not by the
 // shape, so they sit at the same offsets whatever shape uses the workspace.
 constexpr int kMaxCtas = 1024;
-// A split segment's merge ticket counts its finished pieces in bits 0-15, its
-// pieces that met a bad page in bits 16-26 (at most kMaxCtas of them), and in
-// bits 27-30 the merging CTAs that have seen the count complete (when several
-// CTAs share the final merge).
+// Each split segment has two ticket words, indexed by the CTA holding its
+// first page: tickets[i] and tickets[kMaxCtas + i].
+//  * In-kernel merge (merge_mode 0): the first word counts the pieces that
+//    have arrived (bits 0-15; taken as soon as a CTA's pages are done, the
+//    old count giving the piece's arrival order) and, in bits 27-30, the
+//    merging CTAs that have seen every piece written (when several CTAs share
+//    the final merge); the second counts the pieces written (bits 0-15,
+//    added with release order after the piece's slot) and those that met a
+//    bad page (bits 16-26).
+//  * Combine kernel (merge_mode 1): the first word counts the pieces written
+//    and the bad ones as above; the combine kernel reads and clears it.
 constexpr int kTicketPoison = 1 << 16;
 constexpr int kTicketRelease = 1 << 27;
 constexpr int kTicketCountMask = kTicketPoison - 1;
@@ -102,7 +109,7 @@ constexpr int kHeaderWords = 16;
 struct WsLayout {
   // header[0] CTAs of the last partial launch (status words written),
   // [1] CTAs holding work, [2] total pages, [3] segments
-  size_t ticket_off;     // int32 [kMaxCtas]: merge tickets, zero between calls
+  size_t ticket_off;     // int32 [2 * kMaxCtas]: merge tickets, zero between calls
   size_t status_off;     // int32 [kMaxCtas]: each CTA's status in the last call
   size_t seg_start_off;  // int32 [nseg + 1]
   size_t seg_bad_off;    // int32 [nseg]: 1 where the context length is invalid
@@ -114,7 +121,7 @@ struct WsLayout {
 __host__ __device__ inline WsLayout ws_layout(long long nseg, long long n_max) {
   WsLayout l;
   l.ticket_off = 4 * kHeaderWords;
-  l.status_off = l.ticket_off + 4 * (size_t)kMaxCtas;
+  l.status_off = l.ticket_off + 8 * (size_t)kMaxCtas;
   l.seg_start_off = l.status_off + 4 * (size_t)kMaxCtas;
   l.seg_bad_off = l.seg_start_off + 4 * (size_t)(nseg + 1);
   l.seg_cc_off = l.seg_bad_off + 4 * (size_t)nseg;
@@ -319,13 +326,13 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* addr) {
   return v;
 }
 
-// Polls a merge ticket (acquire) until its piece count reaches np; returns
-// the word, or -1 once kWaitBudgetNs have passed.
-__device__ __forceinline__ int wait_ticket_count(const int32_t* ticket, int np) {
+// Polls a merge ticket (acquire) until its count reaches n; returns the word,
+// or -1 once kWaitBudgetNs have passed.
+__device__ __forceinline__ int wait_ticket_count(const int32_t* ticket, int n) {
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     const int w = ld_acquire_gpu(ticket);
-    if ((w & kTicketCountMask) == np) return w;
+    if ((w & kTicketCountMask) == n) return w;
     if (global_timer_ns() - t0 > kWaitBudgetNs) return -1;
   }
 }
@@ -336,6 +343,11 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* addr, int v) {
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v)
                : "memory");
   return old;
+}
+
+// Device-scope reduction (no result) with release ordering.
+__device__ __forceinline__ void red_add_release_gpu(int32_t* addr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -220,9 +220,10 @@ def test_plan_matches_oracle_bit_exactly(planner):
 
 
 def _tickets(d: Dev) -> np.ndarray:
-    """The workspace's merge-ticket words (bytes 64 .. 64 + 4*1024)."""
+    """The workspace's merge-ticket words (bytes 64 .. 64 + 8*1024: two per
+    possible CTA)."""
     torch.cuda.synchronize()
-    return d.ws[64:64 + 4 * 1024].cpu().numpy().view(np.int32)
+    return d.ws[64:64 + 8 * 1024].cpu().numpy().view(np.int32)
 
 
 @pytest.mark.parametrize("merge_mode", [0, 1])

@@ -112,7 +112,7 @@ def test_warp_mode_leaves_the_tickets_at_zero(merge_mode):
         d.run()
         out = d.result()
         torch.cuda.synchronize()
-        tickets = d.ws[64:64 + 4 * 1024].cpu().numpy().view(np.int32)
+        tickets = d.ws[64:64 + 8 * 1024].cpu().numpy().view(np.int32)
         assert np.all(tickets == 0)
         if bad:
             assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
