@@ -511,7 +511,7 @@ struct CtaShared {
   // pieces of segments merged by merge_shared: rank (-1: none; 0: the last
   // piece to arrive) and merging CTAs
   int pend_rank[2], pend_nh[2];
-  int arrived[2];  // old arrival counts of the range's first and last segment
+  int arrived[2];  // old arrival counts of the range's first and last segment (-1: none)
   int wait_word;  // the ticket word a helper saw complete (-1: it did not)
   int npend;
   // the range's first and last segment (the only ones a range can share with
@@ -1264,12 +1264,16 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
   consumer_bar();
   stamp(4);
   // In-kernel merge: the arrival tickets of the range's split segments (its
-  // first and last; thread e takes segment e) are taken now, so that their
-  // round trip overlaps the merges of the buffered segments below.
-  int arrived = 0;
+  // first and last; thread e takes segment e) that are merged by arrival
+  // order (see below) are taken now, so that their round trip overlaps the
+  // merges of the buffered segments.
+  int arrived = -1;  // -1: merged by the piece written last (no arrival ticket)
   if (p.fused_merge && tid < 2 && (tid == 0 || sh.own_seg[1] != sh.own_seg[0]) &&
-      sh.own_ilo[tid] != sh.own_ihi[tid])
-    arrived = atomicAdd(&p.tickets[sh.own_ilo[tid]], 1);
+      sh.own_ilo[tid] != sh.own_ihi[tid]) {
+    const int sg = sh.own_seg[tid], np = sh.own_ihi[tid] - sh.own_ilo[tid] + 1;
+    if (np > kAlone || (np <= kFewPieces && rv.segs[sg + 1] - rv.segs[sg] >= kArriveFirstPages))
+      arrived = atomicAdd(&p.tickets[sh.own_ilo[tid]], 1);
+  }
   for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k)
     merge_buffer<NT>(p, sh, sm.merge_bufs, k % kBufs, ncols, v_scale);
   if (tid < 2) sh.arrived[tid] = arrived;
@@ -1284,13 +1288,15 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
       // page (unique in a call). Each piece raises the written count by 1,
       // plus kTicketPoison if it met a bad page, with release order after its
       // slot. In-kernel merge, by the piece count:
-      //  * at most kFewPieces: the last piece to arrive (arrival rank 0)
-      //    merges alone once every other piece is written (acquire through
-      //    the written count; it does not raise it), then clears both words;
-      //  * up to kAlone: the piece that completes the written count (its
-      //    atomic returns the count and the bad flags) merges alone and
-      //    clears both words (the pieces' arrivals are close together here:
-      //    the last to arrive would often wait for another's slot);
+      //  * at most kFewPieces, of a segment of at least kArriveFirstPages
+      //    pages: the last piece to arrive (arrival rank 0) merges alone once
+      //    every other piece is written (acquire through the written count;
+      //    it does not raise it), then clears both words;
+      //  * other segments of up to kAlone pieces: the piece that completes
+      //    the written count (its atomic returns the count and the bad
+      //    flags) merges alone and clears both words (their pieces finish
+      //    close together: the last to arrive would often wait for another's
+      //    slot);
       //  * more: merge_shared, by the last nh pieces to arrive.
       // Combine kernel: the first word takes the written counts; the combine
       // kernel reads and clears it.
@@ -1307,13 +1313,12 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
           if (r < nh) rank = r;
           red_add_release_gpu(written, add);
           sh.pend_nh[tid] = nh;
-        } else if (np > kFewPieces) {
+        } else if (sh.arrived[e] < 0) {
           const int old = atom_add_acq_rel_gpu(written, add);
           if ((old & kTicketCountMask) == np - 1) {
             last = 1;
             bad = ((old & kTicketPoisonMask) != 0 || add > 1) ? 1 : 0;
-            p.tickets[ilo] = 0;  // every piece arrived before raising the written count
-            *written = 0;
+            *written = 0;  // (the arrival word is not used for these segments)
           }
         } else if (r == 0) {
           const int w = wait_ticket_count(written, np - 1);  // the other pieces' slots

@@ -252,6 +252,27 @@ def test_merge_tickets_are_zero_after_every_call(merge_mode):
     assert_close(d.result(), ref, "after the bad calls")
 
 
+@pytest.mark.parametrize("merge_mode", [0, 1])
+def test_long_segments_of_few_pieces_with_a_bad_page(merge_mode):
+    # segments of 563 and 750 pages split into 2-3 pieces over 8 CTAs: the
+    # last piece to arrive merges them; a bad block id in one must give NaN
+    # in its rows only, and every call must leave the tickets at zero
+    w = wl.make_custom([9000, 12000, 40], 8, 2, seed=75)
+    ref = oracle_of(w)
+    d = Dev(w, max_ctas=8, merge_mode=merge_mode)
+    d.run()
+    assert d.status() == xqa.XQA_OK
+    assert np.all(_tickets(d) == 0)
+    assert_close(d.result(), ref, "long segments, few pieces")
+    d.bt[1, 400] = w.num_blocks + 2
+    d.run()
+    assert d.status() == xqa.XQA_ERR_BAD_BLOCK_ID
+    out = d.result()
+    assert np.all(np.isnan(out[1].astype(np.float32)))
+    assert_close(out[[0, 2]], ref[[0, 2]], "beside the bad sequence")
+    assert np.all(_tickets(d) == 0)
+
+
 @pytest.mark.parametrize("hq,hkv,q_len", [(8, 1, 1), (16, 1, 1), (4, 1, 1), (8, 2, 2), (32, 4, 1)])
 def test_final_merge_shared_by_the_last_ctas(hq, hkv, q_len):
     # long sequences over one CTA per SM: a segment of many pieces is merged by
