@@ -1245,13 +1245,12 @@ __device__ __noinline__ void merge_shared(const PartialParams& p, CtaShared<NT>&
 }
 
 // End of a CTA's range: the merges still buffered (the range's last kBufs
-// segments, in order), then for each split piece its bad flag and merge
-// ticket, and the merge of every segment this CTA completes. The ticket (a
-// device-wide atomic round trip) is taken once per piece after the whole
-// range, so no mid-range segment boundary stalls the CTA on it; the CTA whose
-// ticket completes a segment merges all its pieces in slot order, exactly as
-// the combine kernel would. Last, after an abort, the copies still in flight
-// are waited for.
+// segments, in order), then for each split piece (at most two: the range's
+// first and last segment) its merge tickets, and the final merges this CTA
+// takes part in (all pieces in slot order, exactly as the combine kernel
+// would). The tickets are device-wide atomic round trips taken once per piece
+// after the whole range, so no mid-range segment boundary stalls the CTA on
+// them. Last, after an abort, the copies still in flight are waited for.
 template <int NT>
 __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<NT>& sh,
                                              const CtaSmem<NT>& sm, const RangeView& rv,
