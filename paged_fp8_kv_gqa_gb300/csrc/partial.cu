@@ -1270,7 +1270,8 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
   if (p.fused_merge && tid < 2 && (tid == 0 || sh.own_seg[1] != sh.own_seg[0]) &&
       sh.own_ilo[tid] != sh.own_ihi[tid]) {
     const int sg = sh.own_seg[tid], np = sh.own_ihi[tid] - sh.own_ilo[tid] + 1;
-    if (np > kAlone || (np <= kFewPieces && rv.segs[sg + 1] - rv.segs[sg] >= kArriveFirstPages))
+    if (np > kAlone ||
+        (np <= kArriveFirstPieces && rv.segs[sg + 1] - rv.segs[sg] >= kArriveFirstPages))
       arrived = atomicAdd(&p.tickets[sh.own_ilo[tid]], 1);
   }
   for (int k = kseg > kBufs ? kseg - kBufs : 0; k < kseg; ++k)
@@ -1287,8 +1288,9 @@ __device__ __forceinline__ void finish_range(const PartialParams& p, CtaShared<N
       // page (unique in a call). Each piece raises the written count by 1,
       // plus kTicketPoison if it met a bad page, with release order after its
       // slot. In-kernel merge, by the piece count:
-      //  * at most kFewPieces, of a segment of at least kArriveFirstPages
-      //    pages: the last piece to arrive (arrival rank 0) merges alone once
+      //  * at most kArriveFirstPieces, of a segment of at least
+      //    kArriveFirstPages pages: the last piece to arrive (arrival rank 0)
+      //    merges alone once
       //    every other piece is written (acquire through the written count;
       //    it does not raise it), then clears both words;
       //  * other segments of up to kAlone pieces: the piece that completes

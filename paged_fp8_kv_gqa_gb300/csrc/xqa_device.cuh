@@ -56,10 +56,12 @@ constexpr int kSegCost = 32;
 // Larger segments are merged by several CTAs, gathered in shared memory.
 constexpr int kFewPieces = 6;  // covers the 5-6 pieces of 16K-token segments on 152 SMs
 constexpr int kWidePieces = 16;
-// A split segment of at most kFewPieces pieces and at least this many pages is
-// merged by the last piece to arrive (its long pieces finish at spread-out
-// times); shorter ones by the piece written last (their pieces finish nearly
-// together, and the last to arrive would wait for another's slot).
+// A split segment of at most kArriveFirstPieces pieces and at least
+// kArriveFirstPages pages is merged by the last piece to arrive (its long
+// pieces finish at spread-out times); other segments of up to kWidePieces by
+// the piece written last (their pieces finish nearly together, and the last
+// to arrive would wait for another's slot).
+constexpr int kArriveFirstPieces = 4;
 constexpr int kArriveFirstPages = 512;
 // Warp mode of the partial kernel: a CTA range of at least this many segment
 // pieces, none longer than kWarpModePages pages, gives whole pieces to warps.
