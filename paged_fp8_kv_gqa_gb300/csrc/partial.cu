@@ -593,6 +593,18 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
     prefetch_tensormap(tm_k);
     prefetch_tensormap(tm_v);
   }
+  // Also before the wait, and only a hint: the first pages this CTA index
+  // streamed in the previous call (usually the same pages), fetched into L2
+  // so that the first loads after the wait find them there. The hint words
+  // may be being written by that call; any value is harmless (a row outside
+  // the tensor fetches nothing).
+  if (p.hints != nullptr && tid < kHintPages) {
+    const int y = ld_relaxed_gpu(p.hints + (size_t)cta * kHintPages + tid);
+    if (y >= 0) {
+      tma_prefetch_2d(tm_k, 0, y);
+      tma_prefetch_2d(tm_v, 0, y);
+    }
+  }
   // Every input (and the planner's table, when it ran) is read after the
   // kernels before this one on the stream have completed; this kernel may have
   // become resident while they still ran (programmatic dependent launch).
@@ -984,6 +996,8 @@ __device__ __forceinline__ void cta_mode_range(const PartialParams& p, const CUt
   PageBatch cur = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 0, lane);
   PageBatch nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 32, lane);
   stamp_after(11, cur.y ^ nxt.y);
+  if (p.hints != nullptr && lane < 2)  // this warp's first pair, for the next call's prefetch
+    p.hints[(size_t)blockIdx.x * kHintPages + 2 * warp + lane] = lane < owned && !cur.bad ? cur.y : -1;
   int cur_base = 0;
   auto issue_next = [&]() {
     if (issued >= owned) return;

@@ -224,6 +224,8 @@ xqa_status_t attend_partial_impl(const void* q, const uint8_t* k_cache, const ui
   p.tickets = reinterpret_cast<int32_t*>(base + r.ws.ticket_off);
   p.status = reinterpret_cast<int32_t*>(base + r.ws.status_off);
   p.partials = reinterpret_cast<float*>(base + r.ws.partials_off);
+  p.hints = r.kv_layout == XQA_LAYOUT_HND ? reinterpret_cast<int32_t*>(base + r.ws.hint_off)
+                                          : nullptr;
   p.n_max = r.n_max;
   p.min_pages = r.min_pages;
   p.fused_merge = r.merge_mode == 0 ? 1 : 0;
@@ -375,7 +377,7 @@ xqa_status_t xqa_read_status(const void* workspace, int32_t* device_status, void
   const xqa::WsLayout lay = xqa::ws_layout(0, 0);
   static_assert(xqa::kMaxCtas <= 1024, "status region copied through the stack");
   int32_t words[xqa::kHeaderWords + 3 * xqa::kMaxCtas];
-  if (cudaMemcpyAsync(words, workspace, lay.seg_start_off, cudaMemcpyDeviceToHost, s) !=
+  if (cudaMemcpyAsync(words, workspace, lay.hint_off, cudaMemcpyDeviceToHost, s) !=
           cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return XQA_ERR_LAUNCH;

@@ -112,12 +112,18 @@ static_assert(kMaxCtas * (long long)kTicketPoison < kTicketRelease, "poison bits
 constexpr int kMergeHelpers = 8;
 static_assert(kMergeHelpers * (long long)kTicketRelease <= 0x7fffffffLL + 1, "release bits overflow");
 constexpr int kHeaderWords = 16;
+// Pages of a CTA's range (each warp's first pair, HND caches) whose tensor
+// rows the CTA records for the next call: that call's CTA of the same index
+// prefetches them into L2 while it waits for the kernels before it (a hint:
+// consecutive calls, e.g. the layers of one decode step, cut the same pages).
+constexpr int kHintPages = 2 * 8;
 
 struct WsLayout {
   // header[0] CTAs of the last partial launch (status words written),
   // [1] CTAs holding work, [2] total pages, [3] segments
   size_t ticket_off;     // int32 [2 * kMaxCtas]: merge tickets, zero between calls
   size_t status_off;     // int32 [kMaxCtas]: each CTA's status in the last call
+  size_t hint_off;       // int32 [kMaxCtas * kHintPages]: first pages of each CTA's last range
   size_t seg_start_off;  // int32 [nseg + 1]
   size_t seg_bad_off;    // int32 [nseg]: 1 where the context length is invalid
   size_t seg_cc_off;     // int32 [nseg]: cost of segments 0..s (inclusive), see seg_cost
@@ -129,7 +135,8 @@ __host__ __device__ inline WsLayout ws_layout(long long nseg, long long n_max) {
   WsLayout l;
   l.ticket_off = 4 * kHeaderWords;
   l.status_off = l.ticket_off + 8 * (size_t)kMaxCtas;
-  l.seg_start_off = l.status_off + 4 * (size_t)kMaxCtas;
+  l.hint_off = l.status_off + 4 * (size_t)kMaxCtas;
+  l.seg_start_off = l.hint_off + 4 * (size_t)kMaxCtas * kHintPages;
   l.seg_bad_off = l.seg_start_off + 4 * (size_t)(nseg + 1);
   l.seg_cc_off = l.seg_bad_off + 4 * (size_t)nseg;
   size_t end = l.seg_cc_off + 4 * (size_t)nseg;
@@ -206,6 +213,22 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 // later async-proxy (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// L2 prefetch of one 2-D tensor tile (coordinates outside the tensor fetch
+// nothing; no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+// Device-scope relaxed load (a value another kernel may be writing).
+__device__ __forceinline__ int ld_relaxed_gpu(const int32_t* addr) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

@@ -52,10 +52,10 @@ def test_host_validation_without_device(lib):
     n = ctypes.c_size_t(0)
     assert lib.xqa_workspace_size(ctypes.byref(shape), ctypes.byref(n)) == xqa.XQA_OK
     nseg = 64
-    # header, merge tickets (two words per CTA) and status words (fixed size:
-    # 1024 CTAs at most), then segment starts, bad-context flags and the
-    # cost-line prefix
-    head = 64 + 8 * 1024 + 4 * 1024 + 4 * (nseg + 1) + 4 * nseg + 4 * nseg
+    # header, merge tickets (two words per CTA), status words and first-page
+    # hints (16 per CTA) (fixed size: 1024 CTAs at most), then segment starts,
+    # bad-context flags and the cost-line prefix
+    head = 64 + 8 * 1024 + 4 * 1024 + 4 * 16 * 1024 + 4 * (nseg + 1) + 4 * nseg + 4 * nseg
     head = (head + 255) // 256 * 256
     assert n.value == head + (152 + nseg) * (16 * 128 + 32) * 4
     for bad in (
