@@ -127,8 +127,11 @@ xqa_status_t xqa_kernels_per_call(const xqa_shape_t* shape, int32_t* kernels);
  *   v_scale       per-tensor V scale
  *   out           device, fp16, same shape as q, contiguous, 16-byte aligned
  *   workspace     device, >= xqa_workspace_size bytes, 256-byte aligned; holds
- *                 the plan, the split partials, the merge tickets and the
- *                 status words. Zero-fill it once before its first use (e.g.
+ *                 the plan, the split partials, the merge tickets, the
+ *                 status words and each CTA's first pages of the last call
+ *                 (a prefetch hint for the next call: any content is safe,
+ *                 results never depend on it). Zero-fill it once before its
+ *                 first use (e.g.
  *                 cudaMemsetAsync(workspace, 0, bytes)): every call leaves the
  *                 tickets at zero for the next. The tickets and status words
  *                 sit at fixed offsets, so one workspace may serve calls of

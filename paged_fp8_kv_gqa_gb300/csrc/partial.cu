@@ -1647,8 +1647,9 @@ cudaError_t launch_partial(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const PartialParams& p, int n_max, cudaStream_t stream) {
   // Programmatic dependent launch: CTAs may become resident while the previous
   // kernel on the stream (the planner, or whatever the caller ran before)
-  // still runs; each waits for it with griddepcontrol.wait before reading or
-  // writing global memory.
+  // still runs; each waits for it with griddepcontrol.wait before reading its
+  // inputs or writing global memory (before the wait it reads only its
+  // first-page hints, to prefetch pages into L2).
   const int nt = (p.group * p.q_len + 7) / 8;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_max);
