@@ -601,8 +601,14 @@ __device__ __forceinline__ bool setup_range(const PartialParams& p, const CUtens
   if (p.hints != nullptr && tid < kHintPages) {
     const int y = ld_relaxed_gpu(p.hints + (size_t)cta * kHintPages + tid);
     if (y >= 0) {
-      tma_prefetch_2d(tm_k, 0, y);
-      tma_prefetch_2d(tm_v, 0, y);
+      if (p.kv_layout == XQA_LAYOUT_HND) {
+        tma_prefetch_2d(tm_k, 0, y);
+        tma_prefetch_2d(tm_v, 0, y);
+      } else {  // NHD: box (128 dims, 1 kv head, 16 tokens) at (0, kvh, page * 16)
+        const int row = y / kBlockSize, id = row / p.num_kv_heads, kvh = row - id * p.num_kv_heads;
+        tma_prefetch_3d(tm_k, 0, kvh, id * kBlockSize);
+        tma_prefetch_3d(tm_v, 0, kvh, id * kBlockSize);
+      }
     }
   }
   // Every input (and the planner's table, when it ran) is read after the
@@ -996,8 +1002,12 @@ __device__ __forceinline__ void cta_mode_range(const PartialParams& p, const CUt
   PageBatch cur = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 0, lane);
   PageBatch nxt = load_batch(p, segs, s_first, s_hi + 1, cbeg, npages, warp, 32, lane);
   stamp_after(11, cur.y ^ nxt.y);
-  if (p.hints != nullptr && lane < 2)  // this warp's first pair, for the next call's prefetch
-    p.hints[(size_t)blockIdx.x * kHintPages + 2 * warp + lane] = lane < owned && !cur.bad ? cur.y : -1;
+  if (p.hints != nullptr && lane < 2) {  // this warp's first pair, for the next call's prefetch
+    const int row = p.kv_layout == XQA_LAYOUT_HND
+                        ? cur.y
+                        : (cur.y / kBlockSize * p.num_kv_heads + cur.seg % p.num_kv_heads) * kBlockSize;
+    p.hints[(size_t)blockIdx.x * kHintPages + 2 * warp + lane] = lane < owned && !cur.bad ? row : -1;
+  }
   int cur_base = 0;
   auto issue_next = [&]() {
     if (issued >= owned) return;

@@ -224,8 +224,7 @@ xqa_status_t attend_partial_impl(const void* q, const uint8_t* k_cache, const ui
   p.tickets = reinterpret_cast<int32_t*>(base + r.ws.ticket_off);
   p.status = reinterpret_cast<int32_t*>(base + r.ws.status_off);
   p.partials = reinterpret_cast<float*>(base + r.ws.partials_off);
-  p.hints = r.kv_layout == XQA_LAYOUT_HND ? reinterpret_cast<int32_t*>(base + r.ws.hint_off)
-                                          : nullptr;
+  p.hints = reinterpret_cast<int32_t*>(base + r.ws.hint_off);
   p.n_max = r.n_max;
   p.min_pages = r.min_pages;
   p.fused_merge = r.merge_mode == 0 ? 1 : 0;

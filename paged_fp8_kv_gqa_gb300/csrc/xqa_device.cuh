@@ -112,10 +112,11 @@ static_assert(kMaxCtas * (long long)kTicketPoison < kTicketRelease, "poison bits
 constexpr int kMergeHelpers = 8;
 static_assert(kMergeHelpers * (long long)kTicketRelease <= 0x7fffffffLL + 1, "release bits overflow");
 constexpr int kHeaderWords = 16;
-// Pages of a CTA's range (each warp's first pair, HND caches) whose tensor
-// rows the CTA records for the next call: that call's CTA of the same index
-// prefetches them into L2 while it waits for the kernels before it (a hint:
-// consecutive calls, e.g. the layers of one decode step, cut the same pages).
+// Pages of a CTA's range (each warp's first pair) that the CTA records for the
+// next call, as (block id * Hkv + kv head) * 16: that call's CTA of the same
+// index prefetches them into L2 while it waits for the kernels before it (a
+// hint: consecutive calls, e.g. the layers of one decode step, cut the same
+// pages).
 constexpr int kHintPages = 2 * 8;
 
 struct WsLayout {
@@ -221,6 +222,14 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(x), "r"(y)
+               : "memory");
+}
+
+// L2 prefetch of one 3-D tensor tile (as tma_prefetch_2d).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
                : "memory");
 }
 

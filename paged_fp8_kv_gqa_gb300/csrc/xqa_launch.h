@@ -19,8 +19,7 @@ struct PartialParams {
   int32_t* tickets;    // [kMaxCtas] merge tickets of split segments, zero between calls
   int32_t* status;     // [kMaxCtas] each CTA's status in this call
   float* partials;     // [(n_max + nseg) * kSlotFloats]
-  int32_t* hints;      // [kMaxCtas * kHintPages] first pages of each CTA's range (HND;
-                       // null: no hints)
+  int32_t* hints;      // [kMaxCtas * kHintPages] first pages of each CTA's range (null: none)
   int batch, num_q_heads, num_kv_heads, group, max_blocks_per_seq, num_blocks;
   int q_len;                 // new tokens per sequence (q, out: [B, q_len, Hq, D])
   int n_max, min_pages;      // split rule inputs (same values the planner got)
