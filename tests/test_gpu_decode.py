@@ -307,6 +307,45 @@ def test_bad_block_id_in_a_segment_merged_by_several_ctas(merge_mode):
     assert_close(d.result(), ref, "after the bad call")
 
 
+def _hints(d: Dev) -> torch.Tensor:
+    """The workspace's first-page hint words (16 per possible CTA), after the
+    header, the merge tickets and the status words."""
+    off = 64 + 8 * 1024 + 4 * 1024
+    return d.ws[off:off + 4 * 16 * 1024].view(torch.int32)
+
+
+@pytest.mark.parametrize("layout", ["hnd", "nhd"])
+def test_first_page_hints_never_change_results(layout):
+    # the hint words only steer an L2 prefetch before the wait: any content
+    # (negative, huge, rows of other pages) leaves every result bit and the
+    # status unchanged
+    w = workload("b12_boundary")
+    if layout == "nhd":
+        w = wl.to_nhd(w)
+    d = Dev(w)
+    d.run()
+    ref = d.result()
+    assert d.status() == xqa.XQA_OK
+    hints = _hints(d)
+    assert int((hints >= 0).sum()) > 0  # the call recorded its first pages
+    gen = torch.Generator().manual_seed(5)
+    for fill in ("random", "max", "zero", "minus_one", "shifted"):
+        if fill == "random":
+            vals = torch.randint(-2**31, 2**31 - 1, (hints.numel(),), generator=gen, dtype=torch.int64)
+            hints.copy_(vals.to(torch.int32).to(hints.device))
+        elif fill == "max":
+            hints.fill_(2**31 - 1)
+        elif fill == "zero":
+            hints.zero_()
+        elif fill == "minus_one":
+            hints.fill_(-1)
+        else:  # the hints of other CTAs
+            hints.copy_(torch.roll(hints.clone(), 16 * 5))
+        d.run()
+        assert np.array_equal(d.result().view(np.uint16), ref.view(np.uint16)), fill
+        assert d.status() == xqa.XQA_OK
+
+
 def test_one_workspace_serves_several_shapes():
     # the ticket and status regions sit at fixed offsets, so a workspace sized
     # for the largest shape can be used by calls of different shapes in turn
